@@ -1,0 +1,324 @@
+"""Benchmark: virtual-rank ring AllReduce on one GB300 (busbw and HBM GB/s).
+
+One step = one AllReduce of the whole workload through the C ABI: n = 8
+virtual ranks, 256 MiB of fp32 per rank (2 GiB in, 2 GiB out -- far larger
+than the 129 MB L2, so no flush is needed between steps), op sum, ring,
+Simple protocol, channel count from the library's schedule rule.
+
+Reported (one JSON line on rank 0):
+  value     busbw = algbw * 2(n-1)/n, algbw = bytes per rank / time, summed
+            over GPUs (weak scaling: every GPU runs its own n virtual ranks)
+  roofline  essential HBM bytes 2 n S per launch (read n inputs, write n
+            outputs) / kernel time, against MEASURED_PEAKS.json's hbm_gbs
+  e2e       the same metric with pinned host buffers: H2D of the inputs,
+            the AllReduce, D2H of the outputs, every step
+  cpu_baseline  the CPU oracle replaying the same schedule on a bounded
+            sample of the workload, on the host cores
+`--impl reference` times that oracle alone (the reference arm).
+
+Launch: python bench.py [--gpus N] [--steps K] [--warmup W]; for N > 1 under
+torchrun (one process per GPU, RANK/LOCAL_RANK/WORLD_SIZE from the env).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = {
+    "name": "n8_fp32_sum_ring_simple_256MiB",
+    "nranks": 8,
+    "dtype": "float32",
+    "bytes_per_rank": 256 << 20,
+    "op": "sum",
+    "algo": "ring",
+    "proto": "simple",
+    "max_channels": 32,
+}
+METRIC = "allreduce busbw (n=8 virtual ranks, 256 MiB/rank fp32 sum, ring Simple)"
+ELEM = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def busbw_gbs(bytes_per_rank: int, n: int, seconds: float) -> float:
+    """busbw = algbw * 2(n-1)/n with algbw = S / t ("NCCL architecture ...",
+    introduction: the ring moves 2(n-1)/n * S per rank)."""
+    if n == 1:
+        return bytes_per_rank / seconds / 1e9
+    return bytes_per_rank / seconds * 2 * (n - 1) / n / 1e9
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(n: int, dtype: str, op: str, nch: int, chunk_elems: int, count: int) -> dict:
+    """The oracle as it stands, on a bounded sample of the workload."""
+    from oracle import ring as oring
+    from ring_allreduce_reduction_gb300.workloads import make_inputs
+    x = make_inputs(n, count, dtype, "uniform", seed=0)
+    t0 = time.perf_counter()
+    oring.ring_allreduce(x, op, dtype, nch, chunk_elems)
+    dt = time.perf_counter() - t0
+    S = count * ELEM[dtype]
+    return {"value": round(busbw_gbs(S, n, dt), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"n={n} virtual ranks x {count} {dtype} ({S >> 20} MiB/rank), {nch} channel(s), "
+                      f"chunk {chunk_elems} elements, numpy step machine, single thread, {dt:.1f} s"}
+
+
+def run_reference(args) -> int:
+    """Reference arm: the CPU oracle on host cores (rank 0 only)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    W = WORKLOAD
+    n, dtype = W["nranks"], W["dtype"]
+    count = args.ref_count
+    nch, chunk = 1, 32768
+    from oracle import ring as oring
+    from ring_allreduce_reduction_gb300.workloads import make_inputs
+    x = make_inputs(n, count, dtype, "uniform", seed=0)
+    for _ in range(args.warmup):
+        oring.ring_allreduce(x, W["op"], dtype, nch, chunk)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oring.ring_allreduce(x, W["op"], dtype, nch, chunk)
+        times.append(time.perf_counter() - t0)
+    t = max(times) if times else float("nan")
+    S = count * ELEM[dtype]
+    v = busbw_gbs(S, n, statistics.mean(times))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": W["name"] + f" (bounded sample: {S >> 20} MiB/rank)", "nranks": n,
+                   "bytes_per_rank": S, "op": W["op"], "algo": "ring", "channels": nch, "chunk_elems": chunk},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"n={n} x {count} {dtype} per rank, per step; worst step {t:.2f} s"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-count", type=int, default=1 << 22, help="elements per rank of the CPU sample")
+    ap.add_argument("--ref-count", type=int, default=1 << 21, help="elements per rank per reference step")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from ring_allreduce_reduction_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from ring_allreduce_reduction_gb300 import vrccl as v
+    from ring_allreduce_reduction_gb300.workloads import make_inputs
+
+    W = WORKLOAD
+    n, dtype = W["nranks"], W["dtype"]
+    S = W["bytes_per_rank"]
+    count = S // ELEM[dtype]
+    x = make_inputs(n, count, dtype, "uniform", seed=1000 + rank)
+    send = torch.from_numpy(x).cuda()
+    recv = torch.empty_like(send)
+    sp, rp = [send[r] for r in range(n)], [recv[r] for r in range(n)]
+    comm = v.vrcclCommInit(n, W["max_channels"])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        v.vrcclAllReduce(sp, rp, count, dtype, W["op"], W["algo"], W["proto"], comm, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sched = v.vrcclCommGetLastSchedule(comm)
+    shape = v.vrcclCommGetLaunchShape(comm)
+    err = v.vrcclCommGetAsyncError(comm)
+    if err:
+        raise RuntimeError(f"device error during warm-up: {v.RESULTS[err]}")
+
+    # ---- timed region: device-resident inputs
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    err = v.vrcclCommGetAsyncError(comm)
+    if err:
+        raise RuntimeError(f"device error in the timed region: {v.RESULTS[err]}")
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = busbw_gbs(S, n, ms_step / 1e3) * world
+
+    # roofline of the one kernel: essential bytes / mean launch time
+    algo_bytes = 2 * n * S
+    mean_kern_s = statistics.mean(kern_ms) / 1e3
+    peak, peak_kind = measured_peak()
+    achieved = algo_bytes / mean_kern_s / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                "algorithmic_bytes_per_launch": algo_bytes}
+
+    # ---- end to end through the public API with pinned host buffers
+    host_in = torch.from_numpy(x).pin_memory()
+    host_out = torch.empty_like(host_in).pin_memory()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        send.copy_(host_in, non_blocking=True)
+        step()
+        host_out.copy_(recv, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(busbw_gbs(S, n, e2e_ms / 1e3) * world, 3), "unit": "GB/s",
+           "h2d_bytes_per_step": n * S, "d2h_bytes_per_step": n * S, "ms_per_step": round(e2e_ms, 3)}
+
+    v.vrcclCommDestroy(comm)
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu:
+        cpu = cpu_baseline(n, dtype, W["op"], 1, sched["chunk_elems"], args.cpu_count)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": W["name"], "nranks": n, "bytes_per_rank": S, "count": count, "op": W["op"],
+                   "algo": sched["algo"], "proto": sched["proto"], "channels": sched["nchannels"],
+                   "chunk_elems": sched["chunk_elems"], "blocks": shape["blocks"], "threads": shape["threads"],
+                   "slice_elems": shape["slice_elems"],
+                   "l2": "inputs larger than L2 (n*S = 2 GiB in, 2 GiB out); no flush",
+                   "algbw_gbs": round(S / (ms_step / 1e3) / 1e9 * world, 3)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

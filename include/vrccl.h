@@ -1,0 +1,273 @@
+/*
+ * vrccl -- ring AllReduce over n virtual ranks resident in one GPU's memory.
+ *
+ * C ABI of libvrccl.so. Plain C: no CUDA, C++ or torch types appear here;
+ * a CUDA stream is passed as an opaque pointer (a cudaStream_t cast to
+ * void*, NULL = the legacy default stream), and every buffer is a raw
+ * device address on the communicator's device.
+ *
+ * Sources cited:
+ *   [Deep Dive]    "NCCL Source Code Deep Dive: A GPU Journey of One
+ *                  AllReduce" (aireadcode.com; English edition, chapters
+ *                  1-4; the Japanese edition adds ch.5 tuning and ch.6
+ *                  enqueue).
+ *   [Architecture] "NCCL architecture: topology, channels, algorithms and
+ *                  protocols" (arganzheng.life, part 4 of the series
+ *                  "Communication and interconnect: from NCCL to RDMA").
+ *
+ * What it computes. An AllReduce over n ranks: every rank r contributes
+ * sendbufs[r][0..count) and every rank receives, in recvbufs[r][0..count),
+ * the elementwise op over all n contributions [Deep Dive §1.3]. The ranks
+ * are virtual: n buffers in one GPU's HBM. Each channel owns a contiguous
+ * 16-byte-aligned part of the elements and runs the whole algorithm on it
+ * independently [Deep Dive §2.2; Architecture §6.3]. On a channel the ring
+ * algorithm is a reduce-scatter followed by an all-gather, n-1 steps each,
+ * chunked as RingARAlgorithm::getNextSendAddr describes [Deep Dive §2.3;
+ * Architecture §9.4, runRing]; rank r hands chunks to rank r+1 (mod n)
+ * through staging FIFOs in global memory, synchronised by one of the three
+ * wire protocols Simple, LL and LL128 [Architecture §7.2]. The tree
+ * algorithm reduces up and broadcasts down the double binary tree
+ * [Architecture §5.4, §9.4; Deep Dive ch.4, ncclGetBtree/ncclGetDtree].
+ *
+ * Numerics. Floating ops are computed in binary32 (no contraction) and
+ * rounded (to nearest even) to the element type after every step; int32
+ * sum/prod wrap modulo 2^32. For the ring, an element of chunk j ends up as
+ *   op(...op(op(x[j+1], x[j+2]), x[j+3])..., x[j])        (ranks mod n)
+ * where the first operand is the value that arrived from the previous rank
+ * and max/min keep the first operand on a tie. avg (not an NCCL op on the
+ * pages): floats multiply every input once by 1.0f/n before the sum; int32
+ * divides the wrapped sum by n, truncating toward zero, once per chunk.
+ *
+ * Ordering and concurrency. Every call is asynchronous on its stream and
+ * returns once the work is enqueued [Deep Dive §1.3, "Step 2"]; results are
+ * defined after the stream is synchronised. Calls on one communicator
+ * share its FIFOs: they must be ordered (one stream, or streams ordered by
+ * events); calls that overlap on the GPU are undefined. Different
+ * communicators are independent.
+ *
+ * Errors. Synchronous errors return a code and launch nothing. A device-
+ * side failure (a wait that timed out, or an abort) is reported later by
+ * vrcclCommGetAsyncError; after it the communicator accepts only
+ * vrcclCommGetAsyncError, vrcclCommGetErrorInfo and vrcclCommDestroy
+ * (as a revoked NCCL communicator fails fast, [Deep Dive (Japanese
+ * edition) ch.6, ncclEnqueueCheck step 1]).
+ */
+#ifndef VRCCL_H_
+#define VRCCL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VRCCL_VERSION_MAJOR 0
+#define VRCCL_VERSION_MINOR 1
+
+/* Largest number of virtual ranks one communicator accepts. */
+#define VRCCL_MAX_RANKS 128
+/* Largest channel count (NCCL's MAXCHANNELS, [Architecture §5.2]). */
+#define VRCCL_MAX_CHANNELS 64
+/* FIFO depth per edge and protocol (NCCL_STEPS, [Architecture §6.5]). */
+#define VRCCL_STEPS 8
+
+typedef struct vrcclComm* vrcclComm_t;
+typedef void* vrcclStream_t; /* a cudaStream_t */
+
+/* Result codes, after ncclResult_t [Deep Dive (Japanese edition) ch.5]. */
+typedef enum {
+  vrcclSuccess = 0,
+  vrcclInvalidArgument = 1, /* a bad pointer, size, enum or handle */
+  vrcclInvalidUsage = 2,    /* a valid request this communicator or GPU cannot serve */
+  vrcclInternalError = 3,
+  vrcclCudaError = 4,       /* a CUDA runtime call failed */
+  vrcclTimeout = 5,         /* a device-side wait gave up (asynchronous) */
+  vrcclAborted = 6,         /* vrcclCommAbort was called (asynchronous) */
+  vrcclNumResults = 7
+} vrcclResult_t;
+
+typedef enum {
+  vrcclInt32 = 0,
+  vrcclFloat32 = 1,
+  vrcclBfloat16 = 2,
+  vrcclFloat16 = 3,
+  vrcclNumTypes = 4
+} vrcclDataType_t;
+
+typedef enum {
+  vrcclSum = 0,
+  vrcclProd = 1,
+  vrcclMax = 2,
+  vrcclMin = 3,
+  vrcclAvg = 4,
+  vrcclNumOps = 5
+} vrcclRedOp_t;
+
+/* Schedules [Architecture §7.1]. */
+typedef enum {
+  vrcclAlgoRing = 0,
+  vrcclAlgoTree = 1,
+  vrcclAlgoAuto = 2
+} vrcclAlgo_t;
+
+/* Wire protocols [Architecture §7.2; Deep Dive §2.4]. */
+typedef enum {
+  vrcclProtoSimple = 0, /* slot of raw data, then a released tail counter */
+  vrcclProtoLL = 1,     /* 16-byte lines: 4 B data, 4 B flag, 4 B data, 4 B flag */
+  vrcclProtoLL128 = 2,  /* 128-byte lines: 120 B data, 8 B flag */
+  vrcclProtoAuto = 3
+} vrcclProto_t;
+
+/*
+ * vrcclCommInit -- create a communicator of `nranks` virtual ranks on the
+ * current CUDA device, able to run up to `nchannels` channels.
+ * Model: ncclCommInitAll, one process driving every rank [Deep Dive §1.2].
+ * Allocates, on that device, the FIFOs of every protocol for up to
+ * nchannels channels, their control words and status words (about
+ * 3 * nranks * nchannels * 1.1 MiB), and zeroes them.
+ *   comm      out: the new handle; owned by the caller until
+ *             vrcclCommDestroy.
+ *   nranks    1..VRCCL_MAX_RANKS.
+ *   nchannels 1..VRCCL_MAX_CHANNELS; an upper bound, calls may use fewer.
+ * Errors: vrcclInvalidArgument (null comm, out-of-range sizes);
+ *         vrcclCudaError (no device, allocation failed; nothing is leaked).
+ * Environment, read once here: VRCCL_TIMEOUT_MS (device wait limit,
+ * default 2000), VRCCL_DEBUG=INFO (prints each call's decision line),
+ * VRCCL_PROTO / VRCCL_ALGO (simple|ll|ll128 / ring|tree: what "auto"
+ * resolves to), VRCCL_NCHANNELS (channel count "auto" uses).
+ */
+vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchannels);
+
+/*
+ * vrcclAllReduce -- AllReduce of `count` elements over the communicator's
+ * n virtual ranks, enqueued on `stream` as one kernel launch.
+ * Model: ncclAllReduce(sendbuff, recvbuff, count, datatype, op, comm,
+ * stream) [Deep Dive §1.3], with the n per-rank pointers of a
+ * single-process clique passed together and the algorithm and protocol
+ * selectable per call.
+ *   sendbufs  host array of n device pointers; sendbufs[r] holds `count`
+ *             elements of `dtype`. Read during the call only.
+ *   recvbufs  host array of n device pointers; recvbufs[r] receives
+ *             `count` elements. recvbufs[r] == sendbufs[r] (in place) is
+ *             allowed; any other overlap between the 2n buffers is not.
+ *   count     elements per rank. 0 -> success, nothing launched
+ *             [Deep Dive (Japanese edition) ch.6, taskAppend step 4].
+ *   dtype, op as above.
+ *   algo      ring, tree, or auto (the tuning table's choice).
+ *   proto     simple, ll, ll128, or auto (the tuning table's choice).
+ *   comm      a live communicator.
+ *   stream    cudaStream_t on the communicator's device.
+ * Every pointer must be 16-byte aligned. With n == 1 the result is a
+ * copy of the input (after the avg scale), launched as the same kernel.
+ * Errors: vrcclInvalidArgument (null/misaligned/overlapping pointers, bad
+ * enum, null comm); vrcclInvalidUsage (communicator already failed, or the
+ * forced schedule cannot be made co-resident on this GPU); vrcclCudaError
+ * (launch failure).
+ */
+vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                             vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo,
+                             vrcclProto_t proto, vrcclComm_t comm, vrcclStream_t stream);
+
+/*
+ * vrcclCommSetSchedule -- pin the channel count and chunk size used by
+ * later calls (0 = choose automatically, the default).
+ *   nchannels  0, or 1..the communicator's nchannels.
+ *   chunkBytes 0, or the ring chunk size K*E in bytes: a multiple of 16
+ *              and at most VRCCL_STEPS/2 FIFO slots of the protocol in use
+ *              (ALLREDUCE_CHUNKSTEPS = NCCL_STEPS/2, [Deep Dive (Japanese
+ *              edition) ch.6]); a larger value is clamped at call time.
+ * Errors: vrcclInvalidArgument.
+ */
+vrcclResult_t vrcclCommSetSchedule(vrcclComm_t comm, int nchannels, size_t chunkBytes);
+
+/*
+ * vrcclCommGetLastSchedule -- the schedule the last successful
+ * vrcclAllReduce on this communicator used: algo, proto, channel count
+ * and ring chunk size in elements (K). Any output pointer may be NULL.
+ * With this a checker can replay the exact association order.
+ * Errors: vrcclInvalidArgument (null comm); vrcclInvalidUsage (no call yet).
+ */
+vrcclResult_t vrcclCommGetLastSchedule(vrcclComm_t comm, int* algo, int* proto, int* nchannels,
+                                       size_t* chunkElems);
+
+/*
+ * vrcclCommGetAsyncError -- the communicator's device-side status:
+ * vrcclSuccess, vrcclTimeout or vrcclAborted
+ * [Deep Dive §1.4, ncclCommGetAsyncError]. Does not wait for running
+ * work; reads the status word through an internal stream.
+ * Errors: vrcclInvalidArgument; vrcclCudaError.
+ */
+vrcclResult_t vrcclCommGetAsyncError(vrcclComm_t comm, vrcclResult_t* asyncErr);
+
+/*
+ * vrcclCommGetErrorInfo -- where the first device-side failure happened:
+ * the virtual rank, channel and FIFO step of the wait that gave up (all -1
+ * / 0 when there was none). Any output pointer may be NULL.
+ */
+vrcclResult_t vrcclCommGetErrorInfo(vrcclComm_t comm, int* rank, int* channel, uint64_t* step);
+
+/*
+ * vrcclCommSetTimeout -- device wait limit in milliseconds for later
+ * launches (1..3600000). Every device spin-wait gives up after this long,
+ * records vrcclTimeout and makes every other agent of the launch return.
+ */
+vrcclResult_t vrcclCommSetTimeout(vrcclComm_t comm, uint64_t timeoutMs);
+
+/*
+ * vrcclCommAbort -- raise the communicator's abort word, which every
+ * device wait polls; running and later launches return early and the
+ * communicator reports vrcclAborted [Deep Dive §1.4; Architecture §9.5,
+ * abortFlag]. The communicator must still be destroyed.
+ */
+vrcclResult_t vrcclCommAbort(vrcclComm_t comm);
+
+/*
+ * vrcclCommDestroy -- wait for the communicator's work to finish
+ * (device-synchronising), free everything it allocated, and invalidate
+ * the handle. NULL is accepted and ignored.
+ */
+vrcclResult_t vrcclCommDestroy(vrcclComm_t comm);
+
+/* vrcclCommCount -- the number of virtual ranks [Deep Dive §1.2]. */
+vrcclResult_t vrcclCommCount(vrcclComm_t comm, int* nranks);
+
+/* vrcclGetErrorString -- a static, human-readable name of a result code. */
+const char* vrcclGetErrorString(vrcclResult_t result);
+
+/*
+ * vrcclCommInjectFault -- testing aid: in every later launch, agent
+ * (rank, channel) of the given algorithm returns without doing its work
+ * once it reaches FIFO step `afterSteps` of the launch, so its peers' waits
+ * run out (a flag that nothing sets). rank = -1 clears the fault. Nothing
+ * faults or traps: the launch ends when the waits give up.
+ */
+vrcclResult_t vrcclCommInjectFault(vrcclComm_t comm, int rank, int channel, int afterSteps);
+
+/*
+ * vrcclCommGetLaunchShape -- the launch geometry of the last successful
+ * vrcclAllReduce: CTAs (one per agent), threads per CTA and elements per
+ * FIFO slot. Any output pointer may be NULL.
+ * Errors: vrcclInvalidArgument; vrcclInvalidUsage (no call yet).
+ */
+vrcclResult_t vrcclCommGetLaunchShape(vrcclComm_t comm, int* blocks, int* threads, int* sliceElems);
+
+/*
+ * vrcclCommLoadTuning -- replace the communicator's tuning table with the
+ * entries of a measured table file that match its rank count. NCCL fills
+ * latency/bandwidth tables from constants and takes the smallest predicted
+ * time T = lat + bytes/bw [Architecture §8.2]; this table holds measured
+ * times instead, and algo/proto/channels "auto" take its minimum at the
+ * nearest measured power-of-two size. File format, one entry per line:
+ *   nranks algo proto channels log2bytes sliceBytes microseconds
+ * ('#' starts a comment; algo/proto use the enum values above).
+ *   loaded  out (may be NULL): entries kept.
+ * Errors: vrcclInvalidArgument (null comm/path, unreadable file).
+ */
+vrcclResult_t vrcclCommLoadTuning(vrcclComm_t comm, const char* path, int* loaded);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VRCCL_H_ */

@@ -1,0 +1,224 @@
+// Device-side building blocks: memory-model primitives, bounded waits and
+// the element arithmetic of one reduction step.
+//
+// All parties of a FIFO are agents of one kernel on one GPU, so gpu-scope
+// release/acquire is enough where NCCL uses system-scope fences between
+// GPUs ("NCCL architecture: topology, channels, algorithms and protocols",
+// §7.2, Simple: fence_acq_rel_sys then the tail store).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "vrccl_internal.h"
+
+namespace vrccl {
+
+// ------------------------------------------------------------ memory model
+
+__device__ __forceinline__ unsigned long long ldAcquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ldRelaxed(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void stRelaxed(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void stRelease(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fenceAcqRelGpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned long long globalTimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// LL line access: one 16-byte volatile access carries data and flags
+// together ("NCCL architecture ...", §7.2, LL).
+__device__ __forceinline__ uint4 ldVolatile16(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.volatile.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void stVolatile16(uint4* p, uint4 v) {
+  asm volatile("st.volatile.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Streaming user data (read once / written once) and L2-resident FIFO data.
+__device__ __forceinline__ uint4 ldStream16(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void stStream16(void* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
+__device__ __forceinline__ uint4 ldFifo16(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void stFifo16(void* p, uint4 v) { __stcg(reinterpret_cast<uint4*>(p), v); }
+__device__ __forceinline__ uint2 ldStream8(const void* p) { return __ldcs(reinterpret_cast<const uint2*>(p)); }
+__device__ __forceinline__ void stStream8(void* p, uint2 v) { __stcs(reinterpret_cast<uint2*>(p), v); }
+__device__ __forceinline__ uint2 ldFifo8(const void* p) { return __ldcg(reinterpret_cast<const uint2*>(p)); }
+__device__ __forceinline__ void stFifo8(void* p, uint2 v) { __stcg(reinterpret_cast<uint2*>(p), v); }
+
+// ------------------------------------------------------------ bounded waits
+
+// Records the first failure of the launch and raises the device abort word.
+__device__ __forceinline__ void recordFailure(const DevComm& c, int code, int rank, int ch, int kind,
+                                              unsigned long long step) {
+  if (atomicCAS(&c.status->code, 0, code) == 0) {
+    c.status->rank = rank;
+    c.status->channel = ch;
+    c.status->kind = kind;
+    c.status->step = step;
+  }
+  __threadfence();
+  atomicExch(c.devAbort, 1);
+}
+
+// One spinning thread's budget: every 1024 polls it checks the abort words
+// and the clock; past the communicator's timeout it records vrcclTimeout.
+struct Spin {
+  unsigned long long t0;
+  unsigned n;
+  __device__ __forceinline__ Spin() : t0(0), n(0) {}
+  // true = give up
+  __device__ __forceinline__ bool tick(const DevComm& c, int rank, int ch, int kind, unsigned long long step) {
+    if ((++n & 1023u) != 0) return false;
+    if (*reinterpret_cast<volatile int*>(c.devAbort)) return true;
+    if (*c.hostAbort) {
+      recordFailure(c, vrcclAborted, rank, ch, kind, step);
+      return true;
+    }
+    unsigned long long now = globalTimer();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > c.timeoutNs) {
+      recordFailure(c, vrcclTimeout, rank, ch, kind, step);
+      return true;
+    }
+    return false;
+  }
+};
+
+// Wait until *p >= v (acquire). false = gave up.
+__device__ __forceinline__ bool waitGE(const unsigned long long* p, unsigned long long v, const DevComm& c,
+                                       int rank, int ch, int kind) {
+  Spin s;
+  while (ldAcquire(p) < v) {
+    if (s.tick(c, rank, ch, kind, v)) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool aborted(const DevComm& c) {
+  return *reinterpret_cast<volatile int*>(c.devAbort) != 0 || *c.hostAbort != 0;
+}
+
+// ------------------------------------------------------------ element types
+
+template <int DT> struct Ty;
+template <> struct Ty<vrcclInt32> {
+  using S = int32_t;
+  static constexpr bool kFloat = false;
+};
+template <> struct Ty<vrcclFloat32> {
+  using S = float;
+  static constexpr bool kFloat = true;
+  __device__ static __forceinline__ float toF(float x) { return x; }
+  __device__ static __forceinline__ float fromF(float x) { return x; }
+};
+template <> struct Ty<vrcclBfloat16> {
+  using S = unsigned short;
+  static constexpr bool kFloat = true;
+  __device__ static __forceinline__ float toF(unsigned short x) { return __bfloat162float(__ushort_as_bfloat16(x)); }
+  __device__ static __forceinline__ unsigned short fromF(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  }
+};
+template <> struct Ty<vrcclFloat16> {
+  using S = unsigned short;
+  static constexpr bool kFloat = true;
+  __device__ static __forceinline__ float toF(unsigned short x) { return __half2float(__ushort_as_half(x)); }
+  __device__ static __forceinline__ unsigned short fromF(float x) { return __half_as_ushort(__float2half_rn(x)); }
+};
+
+// One reduction step op(a, b); a is the running value. Floating types: the
+// op in binary32 without contraction, then one rounding to the type; max
+// and min keep `a` on a tie. int32 sum/prod wrap.
+template <int DT, int OP>
+__device__ __forceinline__ typename Ty<DT>::S combine(typename Ty<DT>::S a, typename Ty<DT>::S b) {
+  if constexpr (!Ty<DT>::kFloat) {
+    if constexpr (OP == vrcclSum || OP == vrcclAvg) return int32_t(uint32_t(a) + uint32_t(b));
+    if constexpr (OP == vrcclProd) return int32_t(uint32_t(a) * uint32_t(b));
+    if constexpr (OP == vrcclMax) return b > a ? b : a;
+    if constexpr (OP == vrcclMin) return b < a ? b : a;
+  } else {
+    float fa = Ty<DT>::toF(a), fb = Ty<DT>::toF(b);
+    if constexpr (OP == vrcclSum || OP == vrcclAvg) return Ty<DT>::fromF(__fadd_rn(fa, fb));
+    if constexpr (OP == vrcclProd) return Ty<DT>::fromF(__fmul_rn(fa, fb));
+    if constexpr (OP == vrcclMax) return fb > fa ? b : a;
+    if constexpr (OP == vrcclMin) return fb < fa ? b : a;
+  }
+}
+
+// What a rank feeds into the reduction for its own element (avg scale).
+template <int DT, int OP>
+__device__ __forceinline__ typename Ty<DT>::S prescale(typename Ty<DT>::S x, float scale) {
+  if constexpr (OP == vrcclAvg && Ty<DT>::kFloat) return Ty<DT>::fromF(__fmul_rn(Ty<DT>::toF(x), scale));
+  return x;
+}
+
+// Applied where a chunk becomes final: int32 avg divides, truncating.
+template <int DT, int OP>
+__device__ __forceinline__ typename Ty<DT>::S postop(typename Ty<DT>::S x, int n) {
+  if constexpr (OP == vrcclAvg && !Ty<DT>::kFloat) return x / n;
+  return x;
+}
+
+// ------------------------------------------------------------ packed words
+// A 32-bit word holds one 4-byte element or two 2-byte elements (element 0
+// in the low half, as they sit in memory).
+
+__device__ __forceinline__ int32_t fromWord(uint32_t w, int32_t*) { return int32_t(w); }
+__device__ __forceinline__ float fromWord(uint32_t w, float*) { return __uint_as_float(w); }
+__device__ __forceinline__ uint32_t toWord(int32_t x) { return uint32_t(x); }
+__device__ __forceinline__ uint32_t toWord(float x) { return __float_as_uint(x); }
+
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t combineWord(uint32_t a, uint32_t b) {
+  using S = typename Ty<DT>::S;
+  if constexpr (sizeof(S) == 4) {
+    return toWord(combine<DT, OP>(fromWord(a, (S*)nullptr), fromWord(b, (S*)nullptr)));
+  } else {
+    uint32_t lo = combine<DT, OP>(S(a & 0xffffu), S(b & 0xffffu));
+    uint32_t hi = combine<DT, OP>(S(a >> 16), S(b >> 16));
+    return lo | (hi << 16);
+  }
+}
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t prescaleWord(uint32_t a, float scale) {
+  using S = typename Ty<DT>::S;
+  if constexpr (!(OP == vrcclAvg && Ty<DT>::kFloat)) {
+    return a;
+  } else if constexpr (sizeof(S) == 4) {
+    return toWord(prescale<DT, OP>(fromWord(a, (S*)nullptr), scale));
+  } else {
+    uint32_t lo = prescale<DT, OP>(S(a & 0xffffu), scale);
+    uint32_t hi = prescale<DT, OP>(S(a >> 16), scale);
+    return lo | (hi << 16);
+  }
+}
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t postopWord(uint32_t a, int n) {
+  if constexpr (OP == vrcclAvg && !Ty<DT>::kFloat) return uint32_t(int32_t(a) / n);
+  return a;
+}
+
+}  // namespace vrccl

@@ -1,0 +1,439 @@
+// The agent engine: one CTA is one agent, i.e. one virtual rank working one
+// channel (ring) or one role of one rank in one tree (tree). An agent runs
+// a fixed sequence of FIFO steps ("slices"); each slice receives from up
+// to two in-edges, reduces with the agent's own input, and sends on up to
+// two out-edges and/or writes the agent's recv buffer -- the primitives of
+// "NCCL architecture: topology, channels, algorithms and protocols", §9.4
+// (send / recvReduceSend / recvReduceCopySend / recvCopySend / recv, with
+// Fan = receive/send arity: ring 1/1, tree up to 2/1 and 1/2).
+//
+// Flow control is NCCL's head/tail credit scheme of §6.5 of the same page:
+// a sender may fill slot `step % VRCCL_STEPS` once the receiver's head
+// shows the slot drained (head + VRCCL_STEPS > step). How the receiver
+// learns that data is complete depends on the protocol (§7.2):
+//   Simple  the sender releases a tail counter after the whole slot;
+//   LL      every 16-byte line carries the step number twice next to 8
+//           bytes of data and is written with one 16-byte store;
+//   LL128   every 128-byte line carries 120 data bytes and an 8-byte flag,
+//           released after the line's data (see llSlice128 for why the
+//           flag is a release store here).
+#pragma once
+
+#include "device_common.cuh"
+
+namespace vrccl {
+
+enum SliceFlags : int {
+  F_IN = 1,    // read this agent's input (pre-scaled) into the reduction
+  F_OUT = 2,   // write the result to this agent's recv buffer
+  F_POST = 4,  // apply the post-op (int32 avg)
+  F_RECV = 8,  // receive on every in-edge
+  F_SEND = 16  // send on every out-edge
+};
+
+struct Agent {
+  int rank, ch, proto;
+  int nrecv, nsend;
+  int re[2], se[2];
+  unsigned long long rstep[2], sstep[2];
+  int slices;     // FIFO steps done in this launch (fault injection clock)
+  bool faulty;    // this agent is the injected fault
+
+  __device__ __forceinline__ void init(const DevComm& c, int proto_, int rank_, int ch_) {
+    proto = proto_;
+    rank = rank_;
+    ch = ch_;
+    nrecv = nsend = 0;
+    slices = 0;
+    faulty = (c.faultRank == rank_ && c.faultChannel == ch_);
+  }
+  __device__ __forceinline__ void addRecv(const DevComm& c, int e) {
+    if (e < 0) return;
+    re[nrecv] = e;
+    rstep[nrecv] = ldRelaxed(&c.ctrl[proto][e].head);  // posted by this agent last launch
+    ++nrecv;
+  }
+  __device__ __forceinline__ void addSend(const DevComm& c, int e) {
+    if (e < 0) return;
+    se[nsend] = e;
+    sstep[nsend] = ldRelaxed(&c.ctrl[proto][e].tail);  // posted by this agent last launch
+    ++nsend;
+  }
+  __device__ __forceinline__ bool faultNow(const DevComm& c) const { return faulty && slices >= c.faultAfter; }
+  __device__ __forceinline__ char* slot(const DevComm& c, int e, unsigned long long step) const {
+    return c.fifo[proto] + (size_t(e) * kSteps + size_t(step % kSteps)) * slotBufferBytes(proto);
+  }
+  __device__ __forceinline__ void advance(int flags) {
+    if (flags & F_RECV)
+      for (int i = 0; i < nrecv; ++i) ++rstep[i];
+    if (flags & F_SEND)
+      for (int i = 0; i < nsend; ++i) ++sstep[i];
+    ++slices;
+  }
+  // LL / LL128 keep the sender's step only in registers during a launch;
+  // store it so the next launch continues the flag sequence.
+  __device__ __forceinline__ void finish(const DevComm& c) {
+    if (proto != kSimple && threadIdx.x == 0)
+      for (int i = 0; i < nsend; ++i) stRelaxed(&c.ctrl[proto][se[i]].tail, sstep[i]);
+  }
+};
+
+// Thread 0 waits until every out-edge slot of this step is drained (and,
+// for Simple, every in-edge slot is filled); the CTA then learns the
+// outcome through shared memory. false = give up (abort/timeout/fault).
+__device__ __forceinline__ bool slicePrologue(const DevComm& c, Agent& ag, int flags, bool waitTail, int* smFail) {
+  if (threadIdx.x == 0) {
+    bool ok = !ag.faultNow(c);
+    if (ok && (flags & F_SEND)) {
+      for (int i = 0; i < ag.nsend && ok; ++i) {
+        unsigned long long need = ag.sstep[i] + 1;
+        if (need > (unsigned long long)kSteps)
+          ok = waitGE(&c.ctrl[ag.proto][ag.se[i]].head, need - kSteps, c, ag.rank, ag.ch, 1);
+      }
+    }
+    if (ok && waitTail && (flags & F_RECV)) {
+      for (int i = 0; i < ag.nrecv && ok; ++i)
+        ok = waitGE(&c.ctrl[ag.proto][ag.re[i]].tail, ag.rstep[i] + 1, c, ag.rank, ag.ch, 0);
+    }
+    *smFail = ok ? 0 : 1;
+  }
+  __syncthreads();
+  return *smFail == 0;
+}
+
+// Reduction of one group of NW 32-bit words.
+//   ring order: acc = op(received, own)       (recv first)
+//   tree order: acc = op(op(own, recv0), recv1) (own first, children in order)
+// Without F_IN the received value is copied; without F_RECV the own value is.
+template <int DT, int OP, bool TREE, int NW>
+__device__ __forceinline__ void reduceWords(uint32_t (&acc)[NW], const uint32_t (&x)[NW], const uint32_t (&r0)[NW],
+                                            const uint32_t (&r1)[NW], int flags, int nrecv, float scale, int n) {
+  const bool in = flags & F_IN;
+  const bool rv = (flags & F_RECV) && nrecv > 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    uint32_t own = in ? prescaleWord<DT, OP>(x[w], scale) : 0u;
+    uint32_t v;
+    if constexpr (!TREE) {
+      v = rv ? (in ? combineWord<DT, OP>(r0[w], own) : r0[w]) : own;
+    } else {
+      if (in) {
+        v = own;
+        if (rv) v = combineWord<DT, OP>(v, r0[w]);
+        if (rv && nrecv > 1) v = combineWord<DT, OP>(v, r1[w]);
+      } else {
+        v = r0[w];
+      }
+    }
+    if (flags & F_POST) v = postopWord<DT, OP>(v, n);
+    acc[w] = v;
+  }
+}
+
+// Same on single elements (the ragged end of a buffer).
+template <int DT, int OP, bool TREE>
+__device__ __forceinline__ typename Ty<DT>::S reduceElem(typename Ty<DT>::S x, typename Ty<DT>::S r0,
+                                                         typename Ty<DT>::S r1, int flags, int nrecv, float scale,
+                                                         int n) {
+  using S = typename Ty<DT>::S;
+  const bool in = flags & F_IN;
+  const bool rv = (flags & F_RECV) && nrecv > 0;
+  S own = in ? prescale<DT, OP>(x, scale) : S(0);
+  S v;
+  if constexpr (!TREE) {
+    v = rv ? (in ? combine<DT, OP>(r0, own) : r0) : own;
+  } else {
+    if (in) {
+      v = own;
+      if (rv) v = combine<DT, OP>(v, r0);
+      if (rv && nrecv > 1) v = combine<DT, OP>(v, r1);
+    } else {
+      v = r0;
+    }
+  }
+  if (flags & F_POST) v = postop<DT, OP>(v, n);
+  return v;
+}
+
+// ------------------------------------------------------------------ Simple
+// One slice = one slot of raw elements. Data moves in 16-byte vectors; the
+// ragged end (fewer than 16 bytes at the very end of the user buffer) goes
+// element by element. After the CTA barrier one thread makes the CTA's
+// stores visible at gpu scope (the fence is cumulative over the barrier)
+// and then publishes the new tail / head.
+template <int DT, int OP, bool TREE>
+__device__ bool simpleSlice(const KArgs& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
+  using S = typename Ty<DT>::S;
+  constexpr int V = 16 / sizeof(S);
+  __shared__ int smFail;
+  const DevComm& c = a.comm;
+  if (!slicePrologue(c, ag, flags, true, &smFail)) return false;
+
+  const char* src0 = (flags & F_RECV) && ag.nrecv > 0 ? ag.slot(c, ag.re[0], ag.rstep[0]) : nullptr;
+  const char* src1 = (flags & F_RECV) && ag.nrecv > 1 ? ag.slot(c, ag.re[1], ag.rstep[1]) : nullptr;
+  char* dst0 = (flags & F_SEND) && ag.nsend > 0 ? ag.slot(c, ag.se[0], ag.sstep[0]) : nullptr;
+  char* dst1 = (flags & F_SEND) && ag.nsend > 1 ? ag.slot(c, ag.se[1], ag.sstep[1]) : nullptr;
+
+  const int nv = nelem / V;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    const size_t b = size_t(i) * 16;
+    uint4 xv = make_uint4(0, 0, 0, 0), r0v = xv, r1v = xv;
+    if (flags & F_IN) xv = ldStream16(in + b);
+    if (src0) r0v = ldFifo16(src0 + b);
+    if (src1) r1v = ldFifo16(src1 + b);
+    uint32_t x[4] = {xv.x, xv.y, xv.z, xv.w}, r0[4] = {r0v.x, r0v.y, r0v.z, r0v.w},
+             r1[4] = {r1v.x, r1v.y, r1v.z, r1v.w}, acc[4];
+    reduceWords<DT, OP, TREE, 4>(acc, x, r0, r1, flags, ag.nrecv, a.scale, a.nranks);
+    uint4 av = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+    if (dst0) stFifo16(dst0 + b, av);
+    if (dst1) stFifo16(dst1 + b, av);
+    if (flags & F_OUT) stStream16(out + b, av);
+  }
+  for (int j = nv * V + threadIdx.x; j < nelem; j += blockDim.x) {
+    S x = (flags & F_IN) ? reinterpret_cast<const S*>(in)[j] : S(0);
+    S r0 = src0 ? __ldcg(reinterpret_cast<const S*>(src0) + j) : S(0);
+    S r1 = src1 ? __ldcg(reinterpret_cast<const S*>(src1) + j) : S(0);
+    S v = reduceElem<DT, OP, TREE>(x, r0, r1, flags, ag.nrecv, a.scale, a.nranks);
+    if (dst0) reinterpret_cast<S*>(dst0)[j] = v;
+    if (dst1) reinterpret_cast<S*>(dst1)[j] = v;
+    if (flags & F_OUT) reinterpret_cast<S*>(out)[j] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    fenceAcqRelGpu();
+    if (flags & F_SEND)
+      for (int i = 0; i < ag.nsend; ++i) stRelaxed(&c.ctrl[kSimple][ag.se[i]].tail, ag.sstep[i] + 1);
+    if (flags & F_RECV)
+      for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[kSimple][ag.re[i]].head, ag.rstep[i] + 1);
+  }
+  ag.advance(flags);
+  return true;
+}
+
+// ------------------------------------------------------- 8-byte user units
+// LL and LL128 carry user data in 8-byte units. The last unit of a user
+// buffer may be partial: read and write only its valid elements.
+template <typename S>
+__device__ __forceinline__ uint2 loadUnit(const char* p, int validBytes) {
+  if (validBytes >= 8) return ldStream8(p);
+  uint32_t w[2] = {0u, 0u};
+  for (int e = 0; e < validBytes / int(sizeof(S)); ++e) {
+    S v = reinterpret_cast<const S*>(p)[e];
+    uint32_t bits = sizeof(S) == 4 ? *reinterpret_cast<const uint32_t*>(&v)
+                                   : uint32_t(*reinterpret_cast<const unsigned short*>(&v));
+    const int byte = e * int(sizeof(S));
+    w[byte / 4] |= bits << (8 * (byte % 4));
+  }
+  return make_uint2(w[0], w[1]);
+}
+template <typename S>
+__device__ __forceinline__ void storeUnit(char* p, uint2 v, int validBytes) {
+  if (validBytes >= 8) {
+    stStream8(p, v);
+    return;
+  }
+  const uint32_t w[2] = {v.x, v.y};
+  for (int e = 0; e < validBytes / int(sizeof(S)); ++e) {
+    const int byte = e * int(sizeof(S));
+    uint32_t bits = w[byte / 4] >> (8 * (byte % 4));
+    if constexpr (sizeof(S) == 4) {
+      reinterpret_cast<uint32_t*>(p)[e] = bits;
+    } else {
+      reinterpret_cast<unsigned short*>(p)[e] = (unsigned short)(bits & 0xffffu);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------- LL
+// Line u of a slot carries user bytes [8u, 8u+8) of the slice as
+// {data lo, flag, data hi, flag}, flag = (uint32)(step + 1). A reader spins
+// on the line until both flags equal the expected step; the line's data is
+// then complete (the two halves were written by one 16-byte store). Flags
+// only grow, so slots are never cleared.
+template <int DT, int OP, bool TREE>
+__device__ bool llSlice(const KArgs& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
+  using S = typename Ty<DT>::S;
+  __shared__ int smFail;
+  const DevComm& c = a.comm;
+  if (!slicePrologue(c, ag, flags, false, &smFail)) return false;
+
+  const int nbytes = nelem * int(sizeof(S));
+  const int nu = (nbytes + 7) / 8;
+  const bool rv = (flags & F_RECV) && ag.nrecv > 0;
+  const uint4* src[2] = {nullptr, nullptr};
+  uint32_t rflag[2] = {0u, 0u};
+  if (rv)
+    for (int i = 0; i < ag.nrecv; ++i) {
+      src[i] = reinterpret_cast<const uint4*>(ag.slot(c, ag.re[i], ag.rstep[i]));
+      rflag[i] = uint32_t(ag.rstep[i] + 1);
+    }
+  uint4* dst[2] = {nullptr, nullptr};
+  uint32_t sflag[2] = {0u, 0u};
+  if (flags & F_SEND)
+    for (int i = 0; i < ag.nsend; ++i) {
+      dst[i] = reinterpret_cast<uint4*>(ag.slot(c, ag.se[i], ag.sstep[i]));
+      sflag[i] = uint32_t(ag.sstep[i] + 1);
+    }
+
+  bool fail = false;
+  for (int u = threadIdx.x; u < nu && !fail; u += blockDim.x) {
+    const int valid = min(8, nbytes - 8 * u);
+    uint2 xv = make_uint2(0, 0);
+    if (flags & F_IN) xv = loadUnit<S>(in + 8 * u, valid);
+    uint32_t r[2][2] = {{0u, 0u}, {0u, 0u}};
+    if (rv) {
+      for (int i = 0; i < ag.nrecv && !fail; ++i) {
+        Spin sp;
+        uint4 line;
+        do {
+          line = ldVolatile16(src[i] + u);
+          if (line.y == rflag[i] && line.w == rflag[i]) break;
+          if (sp.tick(c, ag.rank, ag.ch, 2, ag.rstep[i] + 1)) {
+            fail = true;
+            break;
+          }
+        } while (true);
+        r[i][0] = line.x;
+        r[i][1] = line.z;
+      }
+      if (fail) break;
+    }
+    uint32_t x[2] = {xv.x, xv.y}, acc[2];
+    reduceWords<DT, OP, TREE, 2>(acc, x, r[0], r[1], flags, ag.nrecv, a.scale, a.nranks);
+    if (flags & F_SEND)
+      for (int i = 0; i < ag.nsend; ++i) stVolatile16(dst[i] + u, make_uint4(acc[0], sflag[i], acc[1], sflag[i]));
+    if (flags & F_OUT) storeUnit<S>(out + 8 * u, make_uint2(acc[0], acc[1]), valid);
+  }
+  if (fail) smFail = 1;
+  __syncthreads();
+  if (smFail) return false;
+  if (threadIdx.x == 0 && rv)
+    for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[kLL][ag.re[i]].head, ag.rstep[i] + 1);
+  ag.advance(flags);
+  return true;
+}
+
+// ------------------------------------------------------------------- LL128
+// A 128-byte line is eight 16-byte pieces held by eight lanes of a warp; a
+// warp moves four lines per pass. Pieces 0..6 carry 16 user bytes, piece 7
+// carries 8 user bytes and, in its upper half, the 8-byte flag
+// (step + 1); line L of a slice carries user bytes [120 L, 120 L + 120).
+//
+// NCCL relies on NVLink making a 128-byte write visible as a whole, so a
+// reader that sees the flag may trust the rest of the line. Within one
+// GPU's memory hierarchy that is not promised, so here the flag lane
+// publishes the flag with a release store after a warp barrier that orders
+// the other lanes' data stores before it, and the reader's flag lane polls
+// with acquire loads and the warp barrier orders the data loads after it.
+// The line format and its 93.75 % payload are unchanged.
+template <int DT, int OP, bool TREE>
+__device__ bool llSlice128(const KArgs& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
+  using S = typename Ty<DT>::S;
+  __shared__ int smFail;
+  const DevComm& c = a.comm;
+  if (!slicePrologue(c, ag, flags, false, &smFail)) return false;
+
+  const int nbytes = nelem * int(sizeof(S));
+  const int nlines = (nbytes + kLL128DataBytes - 1) / kLL128DataBytes;
+  const bool rv = (flags & F_RECV) && ag.nrecv > 0;
+  const char* src[2] = {nullptr, nullptr};
+  if (rv)
+    for (int i = 0; i < ag.nrecv; ++i) src[i] = ag.slot(c, ag.re[i], ag.rstep[i]);
+  char* dst[2] = {nullptr, nullptr};
+  if (flags & F_SEND)
+    for (int i = 0; i < ag.nsend; ++i) dst[i] = ag.slot(c, ag.se[i], ag.sstep[i]);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int p = lane & 7;
+  const int pieceBytes = p < 7 ? 16 : 8;
+  bool fail = false;
+  for (int g = warp * 4; g < nlines; g += nwarps * 4) {
+    const int line = g + (lane >> 3);
+    const bool active = line < nlines;
+    const int ub = line * kLL128DataBytes + p * 16;  // first user byte of this piece
+    const int valid0 = active ? max(0, min(8, nbytes - ub)) : 0;
+    const int valid1 = (active && p < 7) ? max(0, min(8, nbytes - ub - 8)) : 0;
+    uint32_t x[4] = {0u, 0u, 0u, 0u};
+    if ((flags & F_IN) && valid0 > 0) {
+      uint2 u0 = loadUnit<S>(in + ub, valid0);
+      x[0] = u0.x;
+      x[1] = u0.y;
+      if (valid1 > 0) {
+        uint2 u1 = loadUnit<S>(in + ub + 8, valid1);
+        x[2] = u1.x;
+        x[3] = u1.y;
+      }
+    }
+    uint32_t r[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+    if (rv) {
+      if (active && p == 7) {
+        for (int i = 0; i < ag.nrecv && !fail; ++i) {
+          const unsigned long long* flagp =
+              reinterpret_cast<const unsigned long long*>(src[i] + size_t(line) * 128 + 120);
+          const unsigned long long want = ag.rstep[i] + 1;
+          Spin sp;
+          while (ldAcquire(flagp) != want) {
+            if (sp.tick(c, ag.rank, ag.ch, 3, want)) {
+              fail = true;
+              break;
+            }
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, fail)) {
+        fail = true;
+        break;
+      }
+      __syncwarp();
+      if (active) {
+        for (int i = 0; i < ag.nrecv; ++i) {
+          const char* lp = src[i] + size_t(line) * 128 + p * 16;
+          if (p < 7) {
+            uint4 v = ldFifo16(lp);
+            r[i][0] = v.x; r[i][1] = v.y; r[i][2] = v.z; r[i][3] = v.w;
+          } else {
+            uint2 v = ldFifo8(lp);
+            r[i][0] = v.x; r[i][1] = v.y;
+          }
+        }
+      }
+    }
+    uint32_t acc[4];
+    reduceWords<DT, OP, TREE, 4>(acc, x, r[0], r[1], flags, ag.nrecv, a.scale, a.nranks);
+    if (flags & F_SEND) {
+      if (active) {
+        for (int i = 0; i < ag.nsend; ++i) {
+          char* lp = dst[i] + size_t(line) * 128 + p * 16;
+          if (p < 7) stFifo16(lp, make_uint4(acc[0], acc[1], acc[2], acc[3]));
+          else stFifo8(lp, make_uint2(acc[0], acc[1]));
+        }
+      }
+      __syncwarp();
+      if (active && p == 7)
+        for (int i = 0; i < ag.nsend; ++i)
+          stRelease(reinterpret_cast<unsigned long long*>(dst[i] + size_t(line) * 128 + 120), ag.sstep[i] + 1);
+    }
+    if ((flags & F_OUT) && valid0 > 0) {
+      storeUnit<S>(out + ub, make_uint2(acc[0], acc[1]), valid0);
+      if (valid1 > 0) storeUnit<S>(out + ub + 8, make_uint2(acc[2], acc[3]), valid1);
+    }
+    (void)pieceBytes;
+  }
+  if (fail && lane == 0) smFail = 1;
+  __syncthreads();
+  if (smFail) return false;
+  if (threadIdx.x == 0 && rv)
+    for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[kLL128][ag.re[i]].head, ag.rstep[i] + 1);
+  ag.advance(flags);
+  return true;
+}
+
+template <int PROTO, int DT, int OP, bool TREE>
+__device__ __forceinline__ bool runSlice(const KArgs& a, Agent& ag, const char* in, char* out, int nelem,
+                                         int flags) {
+  if constexpr (PROTO == kSimple) return simpleSlice<DT, OP, TREE>(a, ag, in, out, nelem, flags);
+  if constexpr (PROTO == kLL) return llSlice<DT, OP, TREE>(a, ag, in, out, nelem, flags);
+  if constexpr (PROTO == kLL128) return llSlice128<DT, OP, TREE>(a, ag, in, out, nelem, flags);
+}
+
+}  // namespace vrccl

@@ -1,0 +1,10 @@
+// Kernel instantiations of the LL128 protocol: ring and tree, every element
+// type and reduction op.
+#include "kernels.cuh"
+
+namespace vrccl {
+extern const void* const kRingLL128[4][5];
+extern const void* const kTreeLL128[4][5];
+const void* const kRingLL128[4][5] = VRCCL_KERNEL_ROW(kLL128, ringKernel);
+const void* const kTreeLL128[4][5] = VRCCL_KERNEL_ROW(kLL128, treeKernel);
+}  // namespace vrccl

@@ -1,0 +1,83 @@
+#include "tuner.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "vrccl_internal.h"
+
+namespace vrccl {
+
+int defaultChannels(int proto, size_t bytes, int nranks, int maxChannels) {
+  const size_t threads = proto == kSimple ? 512 : 256;
+  const size_t perThread = proto == kSimple ? 64 : proto == kLL128 ? 8 : size_t(8) * nranks;
+  int nc = maxChannels;
+  while (nc > 1 && bytes < size_t(nc) * threads * perThread) --nc;
+  return nc;
+}
+
+static int log2Bucket(size_t bytes) {
+  int b = 0;
+  while ((size_t(1) << (b + 1)) <= bytes && b < 62) ++b;
+  // round to the nearer power of two
+  if (b < 62 && bytes - (size_t(1) << b) > (size_t(1) << (b + 1)) - bytes) ++b;
+  return b;
+}
+
+Choice Tuner::choose(int nranks, size_t bytes, int maxChannels) const {
+  Choice c{kRing, bytes <= 65536 ? kLL : bytes <= (size_t(2) << 20) ? kLL128 : kSimple, 0, 0, 0};
+  if (table_.empty()) return c;
+  const int want = log2Bucket(bytes);
+  int bestDist = 1 << 30;
+  for (const Entry& e : table_)
+    if (e.nranks == nranks && e.channels <= maxChannels) bestDist = std::min(bestDist, std::abs(e.log2bytes - want));
+  if (bestDist == (1 << 30)) return c;
+  double best = 1e300;
+  for (const Entry& e : table_) {
+    if (e.nranks != nranks || e.channels > maxChannels || std::abs(e.log2bytes - want) != bestDist) continue;
+    // nearest measured size: pick the fastest there; ties keep the first
+    const int target = e.log2bytes;
+    (void)target;
+    if (e.us < best) {
+      best = e.us;
+      c.algo = e.algo;
+      c.proto = e.proto;
+      c.channels = e.channels;
+      c.sliceBytes = e.sliceBytes;
+    }
+  }
+  return c;
+}
+
+int Tuner::load(const char* path, int nranks) {
+  FILE* f = fopen(path, "r");
+  if (!f) return -1;
+  char line[512];
+  int count = 0;
+  while (fgets(line, sizeof(line), f)) {
+    char* hash = strchr(line, '#');
+    if (hash) *hash = 0;
+    Entry e;
+    unsigned long long slice = 0;
+    if (sscanf(line, "%d %d %d %d %d %llu %lf", &e.nranks, &e.algo, &e.proto, &e.channels, &e.log2bytes, &slice,
+               &e.us) == 7) {
+      e.sliceBytes = slice;
+      if (e.nranks == nranks && e.algo >= 0 && e.algo <= 1 && e.proto >= 0 && e.proto <= 2 && e.channels >= 1 &&
+          e.us > 0) {
+        table_.push_back(e);
+        ++count;
+      }
+    }
+  }
+  fclose(f);
+  return count;
+}
+
+void Tuner::loadEnvFile(int nranks) {
+  const char* p = getenv("VRCCL_TUNE_FILE");
+  if (p && *p) load(p, nranks);
+}
+
+}  // namespace vrccl

@@ -1,0 +1,55 @@
+// Schedule choice for algo = auto / proto = auto / channels = auto.
+//
+// NCCL predicts a time per (algorithm, protocol) with T = latency +
+// bytes / bandwidth from constants of its tuning tables and takes the
+// minimum ("NCCL architecture: topology, channels, algorithms and
+// protocols", §8.2, ncclTopoGetAlgoTime). Here the table holds times
+// measured on this GPU for this communicator's rank count: per (algo,
+// proto, channels, slice size) and per power-of-two message size, and the
+// choice is the measured minimum at the nearest size. Without a table the
+// rule below stands in: LL up to 64 KiB, LL128 up to 2 MiB, Simple beyond,
+// and NCCL's channel shrink (§6.4 of the same page).
+#pragma once
+
+#include <cstddef>
+#include <string>
+#include <vector>
+
+namespace vrccl {
+
+struct Choice {
+  int algo;
+  int proto;
+  int channels;       // 0 = use defaultChannels()
+  size_t sliceBytes;  // 0 = protocol default
+  size_t chunkBytes;  // 0 = VRCCL_STEPS/2 slices
+};
+
+// NCCL's rule: start from the maximum and drop channels while each would
+// get less than threads x threadThreshold bytes (thresholds 64 B for
+// Simple, 8 B for LL128, 8 B x n for ring LL).
+int defaultChannels(int proto, size_t bytes, int nranks, int maxChannels);
+
+class Tuner {
+ public:
+  struct Entry {
+    int nranks, algo, proto, channels;
+    int log2bytes;
+    size_t sliceBytes;
+    double us;
+  };
+  Choice choose(int nranks, size_t bytes, int maxChannels) const;
+  // Reads VRCCL_TUNE_FILE if set. Format: one entry per line,
+  // "nranks algo proto channels log2bytes sliceBytes microseconds";
+  // '#' starts a comment.
+  void loadEnvFile(int nranks);
+  int load(const char* path, int nranks);  // entries read, -1 on error
+  void add(const Entry& e) { table_.push_back(e); }
+  void clear() { table_.clear(); }
+  size_t size() const { return table_.size(); }
+
+ private:
+  std::vector<Entry> table_;
+};
+
+}  // namespace vrccl

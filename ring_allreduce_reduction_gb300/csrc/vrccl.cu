@@ -1,0 +1,481 @@
+// Host side of libvrccl: communicator lifecycle, argument checks, schedule
+// choice and the single cooperative launch per AllReduce.
+//
+// Sources cited: "NCCL Source Code Deep Dive: A GPU Journey of One
+// AllReduce" (Deep Dive) and "NCCL architecture: topology, channels,
+// algorithms and protocols" (Architecture).
+#include <cuda_runtime.h>
+#include <unistd.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <sys/syscall.h>
+#include <utility>
+#include <vector>
+
+#include "tuner.h"
+#include "vrccl_internal.h"
+
+using namespace vrccl;
+
+namespace vrccl {
+extern const void* const kRingSimple[4][5];
+extern const void* const kTreeSimple[4][5];
+extern const void* const kRingLL[4][5];
+extern const void* const kTreeLL[4][5];
+extern const void* const kRingLL128[4][5];
+extern const void* const kTreeLL128[4][5];
+
+const void* kernelFor(int algo, int proto, int dtype, int op) {
+  if (dtype < 0 || dtype >= 4 || op < 0 || op >= 5) return nullptr;
+  switch (proto * 2 + algo) {
+    case kSimple * 2 + kRing: return kRingSimple[dtype][op];
+    case kSimple * 2 + kTree: return kTreeSimple[dtype][op];
+    case kLL * 2 + kRing: return kRingLL[dtype][op];
+    case kLL * 2 + kTree: return kTreeLL[dtype][op];
+    case kLL128 * 2 + kRing: return kRingLL128[dtype][op];
+    case kLL128 * 2 + kTree: return kTreeLL128[dtype][op];
+  }
+  return nullptr;
+}
+}  // namespace vrccl
+
+// Sentinels at both ends of the communicator, as ncclComm's startMagic /
+// endMagic (Deep Dive §2.1): a stale or foreign handle fails the check.
+static constexpr uint64_t kMagic = 0x5652434331474233ull;  // "VRCC1GB3"
+
+struct vrcclComm {
+  uint64_t startMagic;
+  int device;
+  int nranks;
+  int maxChannels;
+  int smCount;
+  DevComm dc;
+  void* fifoAlloc[kNumProtos];
+  void* ctrlAlloc;
+  void* statusAlloc;  // DevStatus + devAbort word
+  int* hostAbortPinned;
+  cudaStream_t internal;
+  bool failed;
+  bool aborted;
+  // schedule
+  int forceChannels;
+  size_t forceChunkBytes;
+  int envProto, envAlgo, envChannels;
+  bool debug;
+  bool haveLast;
+  int lastAlgo, lastProto, lastChannels;
+  size_t lastChunk;
+  int lastSlice, lastThreads;
+  // LL / LL128 flags are the low bits of a growing step count: an upper
+  // bound of the steps issued so far decides when to clear the FIFOs.
+  unsigned long long llStepBound[kNumProtos];
+  Tuner tuner;
+  uint64_t endMagic;
+};
+
+static bool validComm(const vrcclComm* c) {
+  return c && c->startMagic == kMagic && c->endMagic == kMagic;
+}
+
+static int envInt(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  return atoi(v);
+}
+
+static int parseProto(const char* v) {
+  if (!v) return -1;
+  std::string s(v);
+  for (auto& ch : s) ch = (char)tolower(ch);
+  if (s == "simple") return kSimple;
+  if (s == "ll") return kLL;
+  if (s == "ll128") return kLL128;
+  return -1;
+}
+static int parseAlgo(const char* v) {
+  if (!v) return -1;
+  std::string s(v);
+  for (auto& ch : s) ch = (char)tolower(ch);
+  if (s == "ring") return kRing;
+  if (s == "tree") return kTree;
+  return -1;
+}
+
+static const char* kAlgoName[2] = {"Ring", "Tree"};
+static const char* kProtoName[3] = {"Simple", "LL", "LL128"};
+static const size_t kElemSize[4] = {4, 4, 2, 2};
+
+static size_t fifoBytes(int proto, int nranks, int maxCh) {
+  return size_t(3) * maxCh * nranks * kSteps * slotBufferBytes(proto);
+}
+
+extern "C" const char* vrcclGetErrorString(vrcclResult_t r) {
+  switch (r) {
+    case vrcclSuccess: return "no error";
+    case vrcclInvalidArgument: return "invalid argument";
+    case vrcclInvalidUsage: return "invalid usage";
+    case vrcclInternalError: return "internal error";
+    case vrcclCudaError: return "CUDA error";
+    case vrcclTimeout: return "device wait timed out";
+    case vrcclAborted: return "communicator aborted";
+    default: return "unknown result code";
+  }
+}
+
+static void freeComm(vrcclComm* c) {
+  for (int p = 0; p < kNumProtos; ++p)
+    if (c->fifoAlloc[p]) cudaFree(c->fifoAlloc[p]);
+  if (c->ctrlAlloc) cudaFree(c->ctrlAlloc);
+  if (c->statusAlloc) cudaFree(c->statusAlloc);
+  if (c->hostAbortPinned) cudaFreeHost(c->hostAbortPinned);
+  if (c->internal) cudaStreamDestroy(c->internal);
+  c->startMagic = c->endMagic = 0;
+  delete c;
+}
+
+extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchannels) {
+  if (!comm) return vrcclInvalidArgument;
+  *comm = nullptr;
+  if (nranks < 1 || nranks > kMaxRanks || nchannels < 1 || nchannels > VRCCL_MAX_CHANNELS)
+    return vrcclInvalidArgument;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return vrcclCudaError;
+  vrcclComm* c = new vrcclComm();
+  memset(static_cast<void*>(c), 0, sizeof(*c));
+  new (&c->tuner) Tuner();
+  c->startMagic = c->endMagic = kMagic;
+  c->device = dev;
+  c->nranks = nranks;
+  c->maxChannels = nchannels;
+  cudaDeviceGetAttribute(&c->smCount, cudaDevAttrMultiProcessorCount, dev);
+  const size_t nEdges = size_t(3) * nchannels * nranks;
+  bool ok = true;
+  for (int p = 0; p < kNumProtos && ok; ++p) {
+    ok = cudaMalloc(&c->fifoAlloc[p], fifoBytes(p, nranks, nchannels)) == cudaSuccess &&
+         cudaMemset(c->fifoAlloc[p], 0, fifoBytes(p, nranks, nchannels)) == cudaSuccess;
+  }
+  ok = ok && cudaMalloc(&c->ctrlAlloc, nEdges * kNumProtos * sizeof(EdgeCtrl)) == cudaSuccess &&
+       cudaMemset(c->ctrlAlloc, 0, nEdges * kNumProtos * sizeof(EdgeCtrl)) == cudaSuccess;
+  ok = ok && cudaMalloc(&c->statusAlloc, 256) == cudaSuccess && cudaMemset(c->statusAlloc, 0, 256) == cudaSuccess;
+  ok = ok && cudaHostAlloc((void**)&c->hostAbortPinned, 64, cudaHostAllocMapped) == cudaSuccess;
+  ok = ok && cudaStreamCreateWithFlags(&c->internal, cudaStreamNonBlocking) == cudaSuccess;
+  int* devAbortHostView = nullptr;
+  if (ok) {
+    *c->hostAbortPinned = 0;
+    ok = cudaHostGetDevicePointer((void**)&devAbortHostView, c->hostAbortPinned, 0) == cudaSuccess;
+  }
+  ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    freeComm(c);
+    return vrcclCudaError;
+  }
+  for (int p = 0; p < kNumProtos; ++p) {
+    c->dc.fifo[p] = static_cast<char*>(c->fifoAlloc[p]);
+    c->dc.ctrl[p] = static_cast<EdgeCtrl*>(c->ctrlAlloc) + p * nEdges;
+  }
+  c->dc.status = static_cast<DevStatus*>(c->statusAlloc);
+  c->dc.devAbort = reinterpret_cast<int*>(static_cast<char*>(c->statusAlloc) + 128);
+  c->dc.hostAbort = devAbortHostView;
+  c->dc.nranks = nranks;
+  c->dc.maxChannels = nchannels;
+  c->dc.faultRank = -1;
+  c->dc.faultChannel = -1;
+  c->dc.faultAfter = 0;
+  long long tmo = envInt("VRCCL_TIMEOUT_MS", 2000);
+  if (tmo < 1) tmo = 2000;
+  c->dc.timeoutNs = (unsigned long long)tmo * 1000000ull;
+  const char* dbg = getenv("VRCCL_DEBUG");
+  c->debug = dbg && (strcasecmp(dbg, "INFO") == 0 || strcasecmp(dbg, "TRACE") == 0);
+  c->envProto = parseProto(getenv("VRCCL_PROTO"));
+  c->envAlgo = parseAlgo(getenv("VRCCL_ALGO"));
+  c->envChannels = std::min(envInt("VRCCL_NCHANNELS", 0), nchannels);
+  c->tuner.loadEnvFile(nranks);
+  *comm = c;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommDestroy(vrcclComm_t comm) {
+  if (!comm) return vrcclSuccess;
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(comm->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  freeComm(comm);
+  cudaSetDevice(prev);
+  return e == cudaSuccess ? vrcclSuccess : vrcclCudaError;
+}
+
+extern "C" vrcclResult_t vrcclCommCount(vrcclComm_t comm, int* nranks) {
+  if (!validComm(comm) || !nranks) return vrcclInvalidArgument;
+  *nranks = comm->nranks;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommSetSchedule(vrcclComm_t comm, int nchannels, size_t chunkBytes) {
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  if (nchannels < 0 || nchannels > comm->maxChannels) return vrcclInvalidArgument;
+  if (chunkBytes % 16) return vrcclInvalidArgument;
+  comm->forceChannels = nchannels;
+  comm->forceChunkBytes = chunkBytes;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommSetTimeout(vrcclComm_t comm, uint64_t timeoutMs) {
+  if (!validComm(comm) || timeoutMs < 1 || timeoutMs > 3600000ull) return vrcclInvalidArgument;
+  comm->dc.timeoutNs = timeoutMs * 1000000ull;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommInjectFault(vrcclComm_t comm, int rank, int channel, int afterSteps) {
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  if (rank < 0) {
+    comm->dc.faultRank = comm->dc.faultChannel = -1;
+    return vrcclSuccess;
+  }
+  if (rank >= comm->nranks || channel < 0 || channel >= comm->maxChannels || afterSteps < 0)
+    return vrcclInvalidArgument;
+  comm->dc.faultRank = rank;
+  comm->dc.faultChannel = channel;
+  comm->dc.faultAfter = afterSteps;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommAbort(vrcclComm_t comm) {
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  *reinterpret_cast<volatile int*>(comm->hostAbortPinned) = 1;
+  comm->aborted = true;
+  return vrcclSuccess;
+}
+
+static vrcclResult_t readStatus(vrcclComm_t comm, DevStatus* st) {
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(comm->device);
+  cudaError_t e = cudaMemcpyAsync(st, comm->dc.status, sizeof(DevStatus), cudaMemcpyDeviceToHost, comm->internal);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(comm->internal);
+  cudaSetDevice(prev);
+  return e == cudaSuccess ? vrcclSuccess : vrcclCudaError;
+}
+
+extern "C" vrcclResult_t vrcclCommGetAsyncError(vrcclComm_t comm, vrcclResult_t* asyncErr) {
+  if (!validComm(comm) || !asyncErr) return vrcclInvalidArgument;
+  DevStatus st;
+  vrcclResult_t r = readStatus(comm, &st);
+  if (r != vrcclSuccess) return r;
+  *asyncErr = st.code ? (vrcclResult_t)st.code : (comm->aborted ? vrcclAborted : vrcclSuccess);
+  if (*asyncErr != vrcclSuccess) comm->failed = true;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommGetErrorInfo(vrcclComm_t comm, int* rank, int* channel, uint64_t* step) {
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  DevStatus st;
+  vrcclResult_t r = readStatus(comm, &st);
+  if (r != vrcclSuccess) return r;
+  if (rank) *rank = st.code ? st.rank : -1;
+  if (channel) *channel = st.code ? st.channel : -1;
+  if (step) *step = st.code ? st.step : 0;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommGetLastSchedule(vrcclComm_t comm, int* algo, int* proto, int* nchannels,
+                                                  size_t* chunkElems) {
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  if (!comm->haveLast) return vrcclInvalidUsage;
+  if (algo) *algo = comm->lastAlgo;
+  if (proto) *proto = comm->lastProto;
+  if (nchannels) *nchannels = comm->lastChannels;
+  if (chunkElems) *chunkElems = comm->lastChunk;
+  return vrcclSuccess;
+}
+
+// ------------------------------------------------------------------ launch
+
+// Blocks of `threads` threads of `fn` that can be resident at once.
+static int residentCapacity(const vrcclComm* c, const void* fn, int threads) {
+  static std::mutex mu;
+  static std::vector<std::pair<std::pair<const void*, int>, int>> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto& e : cache)
+    if (e.first.first == fn && e.first.second == threads) return e.second * c->smCount;
+  int per = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, threads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    per = 0;
+  }
+  cache.push_back({{fn, threads}, per});
+  return per * c->smCount;
+}
+
+static int agentsPerChannel(int algo, int n) { return algo == kRing ? n : 2 * n - 1; }
+
+static bool overlapFree(const void* const* s, void* const* r, int n, size_t bytes) {
+  std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+  iv.reserve(2 * n);
+  for (int i = 0; i < n; ++i) {
+    iv.push_back({(uintptr_t)s[i], (uintptr_t)s[i] + bytes});
+    if (r[i] != s[i]) iv.push_back({(uintptr_t)r[i], (uintptr_t)r[i] + bytes});
+  }
+  std::sort(iv.begin(), iv.end());
+  for (size_t i = 1; i < iv.size(); ++i)
+    if (iv[i].first < iv[i - 1].second) return false;
+  return true;
+}
+
+extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                        vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo,
+                                        vrcclProto_t proto, vrcclComm_t comm, vrcclStream_t stream) {
+  // Argument checks first (ncclEnqueueCheck: CommCheck, then ArgsCheck,
+  // Deep Dive (Japanese edition) ch.6).
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  if ((unsigned)dtype >= (unsigned)vrcclNumTypes || (unsigned)op >= (unsigned)vrcclNumOps ||
+      (unsigned)algo > (unsigned)vrcclAlgoAuto || (unsigned)proto > (unsigned)vrcclProtoAuto)
+    return vrcclInvalidArgument;
+  if (!sendbufs || !recvbufs) return vrcclInvalidArgument;
+  const int n = comm->nranks;
+  for (int r = 0; r < n; ++r) {
+    if (!sendbufs[r] || !recvbufs[r]) return vrcclInvalidArgument;
+    if (((uintptr_t)sendbufs[r] | (uintptr_t)recvbufs[r]) & 15u) return vrcclInvalidArgument;
+  }
+  const size_t E = kElemSize[dtype];
+  if (count > (size_t(1) << 40) / E) return vrcclInvalidArgument;
+  if (!overlapFree(sendbufs, recvbufs, n, count * E)) return vrcclInvalidArgument;
+  if (comm->failed || comm->aborted) return vrcclInvalidUsage;
+  if (count == 0) return vrcclSuccess;  // taskAppend step 4: nothing to do
+
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != comm->device) return vrcclInvalidUsage;
+
+  // ---- schedule: algo, proto, channels, chunk, slice, threads
+  const size_t bytes = count * E;
+  const bool userAlgo = algo != vrcclAlgoAuto, userProto = proto != vrcclProtoAuto;
+  Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels);
+  int A = userAlgo ? (int)algo : (comm->envAlgo >= 0 ? comm->envAlgo : ch.algo);
+  int P = userProto ? (int)proto : (comm->envProto >= 0 ? comm->envProto : ch.proto);
+  if (n == 1) A = kRing;  // a single rank is a local copy (ncclLaunchOneRank)
+  int C = comm->forceChannels ? comm->forceChannels
+        : comm->envChannels   ? comm->envChannels
+        : (ch.channels > 0 ? std::min(ch.channels, comm->maxChannels)
+                           : defaultChannels(P, bytes, n, comm->maxChannels));
+  const bool userChannels = comm->forceChannels || comm->envChannels;
+
+  const void* fn = kernelFor(A, P, dtype, op);
+  if (!fn) return vrcclInternalError;
+  int threads = P == kSimple ? 512 : 256;
+  const int per = agentsPerChannel(A, n);
+  // All agents of a launch wait on each other: they must all be resident.
+  // Shrink the CTA first, then (if the caller left it open) the channels.
+  int cap = residentCapacity(comm, fn, threads);
+  while (cap < per * C && threads > 64) {
+    threads /= 2;
+    cap = residentCapacity(comm, fn, threads);
+  }
+  if (cap < per * C) {
+    if (userChannels) return vrcclInvalidUsage;
+    C = cap / per;
+    if (C < 1) return userAlgo ? vrcclInvalidUsage : vrcclInternalError;
+  }
+
+  // Slice: one FIFO slot. Chunk: VRCCL_STEPS/2 slots (ALLREDUCE_CHUNKSTEPS =
+  // NCCL_STEPS/2, Deep Dive (Japanese edition) ch.6); fewer slots than the
+  // FIFO depth per chunk is what keeps the credit ring deadlock-free.
+  size_t sliceBytes = P == kSimple ? (ch.sliceBytes ? ch.sliceBytes : size_t(32) * 1024) : slotDataBytes(P);
+  sliceBytes = std::min(sliceBytes, slotDataBytes(P));
+  if (P == kLL128) sliceBytes = sliceBytes / 240 * 240;  // whole lines and 16-byte slice starts
+  sliceBytes = std::max<size_t>(sliceBytes / 16 * 16, 16);
+  const int sliceElems = (int)(sliceBytes / E);
+  size_t chunkBytes = comm->forceChunkBytes ? comm->forceChunkBytes : (ch.chunkBytes ? ch.chunkBytes : sliceBytes * (kSteps / 2));
+  chunkBytes = std::min(chunkBytes, sliceBytes * (kSteps / 2));
+  chunkBytes = std::max<size_t>(chunkBytes / 16 * 16, 16);
+  const int chunkElems = (int)(chunkBytes / E);
+
+  // ---- LL/LL128 flag wrap: clear the FIFO and its counters well before a
+  // 32-bit flag could repeat a value still sitting in a slot.
+  if (P != kSimple) {
+    const unsigned long long perCh = (bytes + C - 1) / C / E + 1;
+    const unsigned long long bound = 2ull * n * ((perCh + sliceElems - 1) / sliceElems + 2ull * n + 2);
+    if (comm->llStepBound[P] + bound > (1ull << 31)) {
+      const size_t nEdges = size_t(3) * comm->maxChannels * n;
+      if (cudaMemsetAsync(comm->fifoAlloc[P], 0, fifoBytes(P, n, comm->maxChannels), (cudaStream_t)stream) !=
+              cudaSuccess ||
+          cudaMemsetAsync(comm->dc.ctrl[P], 0, nEdges * sizeof(EdgeCtrl), (cudaStream_t)stream) != cudaSuccess)
+        return vrcclCudaError;
+      comm->llStepBound[P] = 0;
+    }
+    comm->llStepBound[P] += bound;
+  }
+
+  KArgs ka;
+  memset(&ka, 0, sizeof(ka));
+  ka.comm = comm->dc;
+  ka.count = count;
+  ka.nranks = n;
+  ka.nchannels = C;
+  ka.chunkElems = chunkElems;
+  ka.sliceElems = sliceElems;
+  ka.scale = 1.0f / (float)n;
+  for (int r = 0; r < n; ++r) {
+    ka.send[r] = sendbufs[r];
+    ka.recv[r] = recvbufs[r];
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(per * C));
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&ka};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e == cudaErrorCooperativeLaunchTooLarge ? vrcclInvalidUsage : vrcclCudaError;
+  }
+  comm->haveLast = true;
+  comm->lastAlgo = A;
+  comm->lastProto = P;
+  comm->lastChannels = C;
+  comm->lastChunk = chunkElems;
+  comm->lastSlice = sliceElems;
+  comm->lastThreads = threads;
+  if (comm->debug) {
+    char host[64] = {0};
+    gethostname(host, sizeof(host) - 1);
+    fprintf(stderr,
+            "%s:%d:%ld [%d] VRCCL INFO AllReduce: %zu Bytes -> Algo %s proto %s channel{Lo..Hi}={0..%d} "
+            "chunk %zu slice %d threads %d nranks %d\n",
+            host, (int)getpid(), (long)syscall(SYS_gettid), comm->device, bytes, kAlgoName[A], kProtoName[P],
+            C - 1, chunkBytes, sliceElems, threads, n);
+  }
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommGetLaunchShape(vrcclComm_t comm, int* blocks, int* threads, int* sliceElems) {
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  if (!comm->haveLast) return vrcclInvalidUsage;
+  if (blocks) *blocks = agentsPerChannel(comm->lastAlgo, comm->nranks) * comm->lastChannels;
+  if (threads) *threads = comm->lastThreads;
+  if (sliceElems) *sliceElems = comm->lastSlice;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommLoadTuning(vrcclComm_t comm, const char* path, int* loaded) {
+  if (!validComm(comm) || !path) return vrcclInvalidArgument;
+  Tuner t;
+  int k = t.load(path, comm->nranks);
+  if (k < 0) return vrcclInvalidArgument;
+  comm->tuner = t;
+  if (loaded) *loaded = k;
+  return vrcclSuccess;
+}

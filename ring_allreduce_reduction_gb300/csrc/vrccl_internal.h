@@ -1,0 +1,112 @@
+// Internal layout shared by the host library and the sm_103a kernels.
+//
+// Device memory of one communicator (all owned by it, zeroed at init):
+//
+//   fifo[proto]  3 * maxChannels * nranks edges, each VRCCL_STEPS slots of
+//                slotBytes[proto]. Edge e of
+//                  [0, C*n)        ring edge (ch, r):   rank r -> r+1 on ch
+//                  [C*n, 2*C*n)    tree up edge (ch, c): child c -> parent
+//                  [2*C*n, 3*C*n)  tree down edge (ch, c): parent -> child c
+//                (C = maxChannels). A Simple slot holds raw elements; an LL
+//                slot holds 16-byte lines {data lo, flag, data hi, flag}; an
+//                LL128 slot holds 128-byte lines of 120 data bytes and an
+//                8-byte flag in bytes 120..127.
+//   ctrl[proto]  one EdgeCtrl per edge: `tail` is written only by the edge's
+//                sender, `head` only by its receiver, on separate 128-byte
+//                lines (ncclSendMem.head / ncclRecvMem.tail of
+//                "NCCL Source Code Deep Dive", §2.4). tail = slots the sender
+//                has filled, head = slots the receiver has drained; both
+//                only grow, across launches.
+//   status       first device-side failure (code, rank, channel, step).
+//   devAbort     set by the first agent that fails; every wait polls it.
+//   hostAbort    mapped pinned host word raised by vrcclCommAbort.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "vrccl.h"
+
+#ifndef __CUDACC__
+#define __host__
+#define __device__
+#endif
+
+namespace vrccl {
+
+constexpr int kSteps = VRCCL_STEPS;
+constexpr int kMaxRanks = VRCCL_MAX_RANKS;
+constexpr int kNumProtos = 3;
+
+enum ProtoId { kSimple = 0, kLL = 1, kLL128 = 2 };
+enum AlgoId { kRing = 0, kTree = 1 };
+
+// FIFO geometry (buffer bytes per slot) and the data one slot carries.
+constexpr size_t kSimpleSlotBytes = 64 * 1024;  // data bytes per Simple slot (max slice)
+constexpr int kLLSlotLines = 2048;              // 16-byte lines: 8 data bytes each
+constexpr int kLL128SlotLines = 512;            // 128-byte lines: 120 data bytes each
+constexpr int kLL128DataBytes = 120;
+
+__host__ __device__ constexpr size_t slotBufferBytes(int proto) {
+  return proto == kSimple ? kSimpleSlotBytes
+       : proto == kLL     ? size_t(kLLSlotLines) * 16
+                          : size_t(kLL128SlotLines) * 128;
+}
+__host__ __device__ constexpr size_t slotDataBytes(int proto) {
+  return proto == kSimple ? kSimpleSlotBytes
+       : proto == kLL     ? size_t(kLLSlotLines) * 8
+                          : size_t(kLL128SlotLines) * kLL128DataBytes;
+}
+
+struct alignas(128) EdgeCtrl {
+  unsigned long long tail;
+  unsigned long long pad0[15];
+  unsigned long long head;
+  unsigned long long pad1[15];
+};
+static_assert(sizeof(EdgeCtrl) == 256, "EdgeCtrl layout");
+
+struct DevStatus {
+  int code;  // vrcclResult_t of the first failure, 0 = none
+  int rank;
+  int channel;
+  int kind;  // 0 = tail wait, 1 = head wait, 2 = LL line, 3 = LL128 flag
+  unsigned long long step;
+};
+
+struct DevComm {
+  char* fifo[kNumProtos];
+  EdgeCtrl* ctrl[kNumProtos];
+  DevStatus* status;
+  int* devAbort;
+  volatile int* hostAbort;
+  unsigned long long timeoutNs;
+  int nranks;
+  int maxChannels;
+  int faultRank;  // fault injection: agent (faultRank, faultChannel) stops
+  int faultChannel;
+  int faultAfter;  // ... once it reaches this FIFO step of the launch
+};
+
+struct KArgs {
+  DevComm comm;
+  unsigned long long count;
+  int nranks;
+  int nchannels;
+  int chunkElems;  // ring chunk K (elements, multiple of 16 bytes)
+  int sliceElems;  // elements per FIFO step (one slot)
+  float scale;     // avg pre-scale 1.0f / n (binary32)
+  int pad;
+  const void* send[kMaxRanks];
+  void* recv[kMaxRanks];
+};
+
+__host__ __device__ inline int ringEdge(int ch, int r, int n) { return ch * n + r; }
+__host__ __device__ inline int treeUpEdge(int ch, int c, int n, int maxCh) { return maxCh * n + ch * n + c; }
+__host__ __device__ inline int treeDownEdge(int ch, int c, int n, int maxCh) { return 2 * maxCh * n + ch * n + c; }
+
+// Kernel table (defined by the kernel translation units).
+// Returns the __global__ function for (algo, proto, dtype, op) or nullptr.
+const void* kernelFor(int algo, int proto, int dtype, int op);
+
+}  // namespace vrccl

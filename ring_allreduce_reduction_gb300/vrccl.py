@@ -1,0 +1,191 @@
+"""Python binding of libvrccl.so: the C entry points under the same names.
+
+Argument marshalling only -- every step of the AllReduce runs in the
+library's sm_103a kernels. Buffers may be given as torch tensors (their
+``data_ptr()`` is passed) or as raw integer device addresses; streams as
+``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or None (the current
+torch stream).
+
+Importing this module loads ``libvrccl.so`` and raises ImportError if it has
+not been built (``python -m ring_allreduce_reduction_gb300.build``): there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvrccl.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m ring_allreduce_reduction_gb300.build`")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+RESULTS = ["vrcclSuccess", "vrcclInvalidArgument", "vrcclInvalidUsage", "vrcclInternalError",
+           "vrcclCudaError", "vrcclTimeout", "vrcclAborted"]
+DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2, "float16": 3}
+OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
+ALGOS = {"ring": 0, "tree": 1, "auto": 2}
+PROTOS = {"simple": 0, "ll": 1, "ll128": 2, "auto": 3}
+ALGO_NAMES = {v: k for k, v in ALGOS.items()}
+PROTO_NAMES = {v: k for k, v in PROTOS.items()}
+ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+MAX_RANKS = 128
+MAX_CHANNELS = 64
+STEPS = 8
+
+_TORCH_DTYPES = {torch.int32: "int32", torch.float32: "float32", torch.bfloat16: "bfloat16",
+                 torch.float16: "float16"}
+
+_c_int_p = ctypes.POINTER(ctypes.c_int)
+_sig = {
+    "vrcclCommInit": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int],
+    "vrcclAllReduce": [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
+                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p],
+    "vrcclCommSetSchedule": [ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t],
+    "vrcclCommGetLastSchedule": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p, ctypes.POINTER(ctypes.c_size_t)],
+    "vrcclCommGetAsyncError": [ctypes.c_void_p, _c_int_p],
+    "vrcclCommGetErrorInfo": [ctypes.c_void_p, _c_int_p, _c_int_p, ctypes.POINTER(ctypes.c_uint64)],
+    "vrcclCommSetTimeout": [ctypes.c_void_p, ctypes.c_uint64],
+    "vrcclCommAbort": [ctypes.c_void_p],
+    "vrcclCommDestroy": [ctypes.c_void_p],
+    "vrcclCommCount": [ctypes.c_void_p, _c_int_p],
+    "vrcclCommInjectFault": [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int],
+    "vrcclCommGetLaunchShape": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p],
+    "vrcclCommLoadTuning": [ctypes.c_void_p, ctypes.c_char_p, _c_int_p],
+}
+for _name, _args in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+_lib.vrcclGetErrorString.argtypes = [ctypes.c_int]
+_lib.vrcclGetErrorString.restype = ctypes.c_char_p
+
+
+class VrcclError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = RESULTS[code] if 0 <= code < len(RESULTS) else str(code)
+        super().__init__(f"{where}: {self.name} ({vrcclGetErrorString(code)})")
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise VrcclError(code, where)
+
+
+def _ptr(x) -> int:
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, torch.cuda.Stream):
+        return s.cuda_stream
+    return int(s)
+
+
+def _enum(table: dict, v, what: str) -> int:
+    if isinstance(v, int):
+        return v
+    if isinstance(v, torch.dtype) and table is DTYPES:
+        v = _TORCH_DTYPES[v]
+    try:
+        return table[v]
+    except KeyError:
+        raise ValueError(f"unknown {what} {v!r}") from None
+
+
+def vrcclGetErrorString(code: int) -> str:
+    return _lib.vrcclGetErrorString(code).decode()
+
+
+def vrcclCommInit(nranks: int, nchannels: int) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(_lib.vrcclCommInit(ctypes.byref(h), nranks, nchannels), "vrcclCommInit")
+    return h
+
+
+def vrcclAllReduce(sendbufs, recvbufs, count: int, dtype, op, algo="ring", proto="simple", comm=None,
+                   stream=None) -> None:
+    n = len(sendbufs)
+    S = (ctypes.c_void_p * n)(*[_ptr(b) for b in sendbufs])
+    R = (ctypes.c_void_p * len(recvbufs))(*[_ptr(b) for b in recvbufs])
+    _check(_lib.vrcclAllReduce(S, R, count, _enum(DTYPES, dtype, "dtype"), _enum(OPS, op, "op"),
+                               _enum(ALGOS, algo, "algo"), _enum(PROTOS, proto, "proto"), comm,
+                               _stream(stream)), "vrcclAllReduce")
+
+
+def vrcclCommSetSchedule(comm, nchannels: int = 0, chunkBytes: int = 0) -> None:
+    _check(_lib.vrcclCommSetSchedule(comm, nchannels, chunkBytes), "vrcclCommSetSchedule")
+
+
+def vrcclCommGetLastSchedule(comm) -> dict:
+    a, p, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    k = ctypes.c_size_t()
+    _check(_lib.vrcclCommGetLastSchedule(comm, ctypes.byref(a), ctypes.byref(p), ctypes.byref(c),
+                                         ctypes.byref(k)), "vrcclCommGetLastSchedule")
+    return {"algo": ALGO_NAMES[a.value], "proto": PROTO_NAMES[p.value], "nchannels": c.value,
+            "chunk_elems": k.value}
+
+
+def vrcclCommGetLaunchShape(comm) -> dict:
+    b, t, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(_lib.vrcclCommGetLaunchShape(comm, ctypes.byref(b), ctypes.byref(t), ctypes.byref(s)),
+           "vrcclCommGetLaunchShape")
+    return {"blocks": b.value, "threads": t.value, "slice_elems": s.value}
+
+
+def vrcclCommGetAsyncError(comm) -> int:
+    e = ctypes.c_int()
+    _check(_lib.vrcclCommGetAsyncError(comm, ctypes.byref(e)), "vrcclCommGetAsyncError")
+    return e.value
+
+
+def vrcclCommGetErrorInfo(comm) -> dict:
+    r, c = ctypes.c_int(), ctypes.c_int()
+    s = ctypes.c_uint64()
+    _check(_lib.vrcclCommGetErrorInfo(comm, ctypes.byref(r), ctypes.byref(c), ctypes.byref(s)),
+           "vrcclCommGetErrorInfo")
+    return {"rank": r.value, "channel": c.value, "step": s.value}
+
+
+def vrcclCommSetTimeout(comm, timeoutMs: int) -> None:
+    _check(_lib.vrcclCommSetTimeout(comm, timeoutMs), "vrcclCommSetTimeout")
+
+
+def vrcclCommAbort(comm) -> None:
+    _check(_lib.vrcclCommAbort(comm), "vrcclCommAbort")
+
+
+def vrcclCommDestroy(comm) -> None:
+    _check(_lib.vrcclCommDestroy(comm), "vrcclCommDestroy")
+
+
+def vrcclCommCount(comm) -> int:
+    n = ctypes.c_int()
+    _check(_lib.vrcclCommCount(comm, ctypes.byref(n)), "vrcclCommCount")
+    return n.value
+
+
+def vrcclCommInjectFault(comm, rank: int, channel: int = 0, afterSteps: int = 0) -> None:
+    _check(_lib.vrcclCommInjectFault(comm, rank, channel, afterSteps), "vrcclCommInjectFault")
+
+
+def vrcclCommLoadTuning(comm, path: str) -> int:
+    k = ctypes.c_int()
+    _check(_lib.vrcclCommLoadTuning(comm, path.encode(), ctypes.byref(k)), "vrcclCommLoadTuning")
+    return k.value
+
+
+def raw_call(name: str, *args) -> int:
+    """Call a C entry point by name and return its raw result code (tests)."""
+    return getattr(_lib, name)(*args)
+
+
+LIB = _lib
+LIB_PATH = _LIB_PATH

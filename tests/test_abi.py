@@ -1,0 +1,67 @@
+"""The C-ABI library: builds, loads, exports every declared entry point, and
+rejects bad arguments on the host before touching the GPU. No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vrccl.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ring_allreduce_reduction_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:vrcclResult_t|const char\*)\s+(vrccl\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for must in ("vrcclCommInit", "vrcclAllReduce", "vrcclCommGetLastSchedule", "vrcclCommGetAsyncError",
+                 "vrcclCommAbort", "vrcclCommDestroy", "vrcclGetErrorString"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), f"{name} declared in include/vrccl.h but not exported"
+
+
+def test_error_strings(lib):
+    lib.vrcclGetErrorString.restype = ctypes.c_char_p
+    assert lib.vrcclGetErrorString(0) == b"no error"
+    assert lib.vrcclGetErrorString(5) == b"device wait timed out"
+    assert lib.vrcclGetErrorString(99) == b"unknown result code"
+
+
+def test_host_side_argument_checks(lib):
+    h = ctypes.c_void_p()
+    assert lib.vrcclCommInit(None, 4, 1) == 1
+    assert lib.vrcclCommInit(ctypes.byref(h), 0, 1) == 1
+    assert lib.vrcclCommInit(ctypes.byref(h), 129, 1) == 1
+    assert lib.vrcclCommInit(ctypes.byref(h), 4, 0) == 1
+    assert lib.vrcclCommInit(ctypes.byref(h), 4, 65) == 1
+    assert lib.vrcclAllReduce(None, None, 1, 0, 0, 0, 0, None, None) == 1
+    bogus = ctypes.create_string_buffer(4096)  # not a communicator: the magic check rejects it
+    assert lib.vrcclAllReduce(None, None, 1, 0, 0, 0, 0, bogus, None) == 1
+    assert lib.vrcclCommDestroy(None) == 0
+    assert lib.vrcclCommDestroy(bogus) == 1
+    assert lib.vrcclCommAbort(bogus) == 1
+    assert lib.vrcclCommCount(bogus, None) == 1
+
+
+def test_binding_names_match_the_c_names():
+    torch = pytest.importorskip("torch")  # noqa: F841
+    from ring_allreduce_reduction_gb300 import build
+    build.build()
+    from ring_allreduce_reduction_gb300 import vrccl
+    for name in declared():
+        assert hasattr(vrccl, name), f"binding lacks {name}"
