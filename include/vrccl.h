@@ -69,8 +69,10 @@ extern "C" {
 #define VRCCL_MAX_RANKS 128
 /* Largest channel count (NCCL's MAXCHANNELS, [Architecture §5.2]). */
 #define VRCCL_MAX_CHANNELS 64
-/* FIFO depth per edge and protocol (NCCL_STEPS, [Architecture §6.5]). */
-#define VRCCL_STEPS 8
+/* FIFO depth per edge and protocol: slots a sender may fill ahead of its
+ * receiver (NCCL_STEPS is 8, [Architecture §6.5]; one GPU's HBM hop costs a
+ * few microseconds, so twice NCCL's depth keeps ~100 KB in flight per edge). */
+#define VRCCL_STEPS 16
 
 typedef struct vrcclComm* vrcclComm_t;
 typedef void* vrcclStream_t; /* a cudaStream_t */
@@ -135,7 +137,12 @@ typedef enum {
  * Environment, read once here: VRCCL_TIMEOUT_MS (device wait limit,
  * default 2000), VRCCL_DEBUG=INFO (prints each call's decision line),
  * VRCCL_PROTO / VRCCL_ALGO (simple|ll|ll128 / ring|tree: what "auto"
- * resolves to), VRCCL_NCHANNELS (channel count "auto" uses).
+ * resolves to), VRCCL_NCHANNELS (channel count "auto" uses),
+ * VRCCL_SLICE_BYTES (largest Simple FIFO slot to use, bytes; default 16384,
+ * at most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent,
+ * default 8), VRCCL_PREFETCH (input slices a Simple agent pulls into L2
+ * ahead of use, default 0 = off, at most 32), VRCCL_TUNE_FILE (a measured
+ * tuning table, see vrcclCommLoadTuning).
  */
 vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchannels);
 

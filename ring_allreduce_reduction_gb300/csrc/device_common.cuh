@@ -67,6 +67,70 @@ __device__ __forceinline__ void stStream8(void* p, uint2 v) { __stcs(reinterpret
 __device__ __forceinline__ uint2 ldFifo8(const void* p) { return __ldcg(reinterpret_cast<const uint2*>(p)); }
 __device__ __forceinline__ void stFifo8(void* p, uint2 v) { __stcg(reinterpret_cast<uint2*>(p), v); }
 
+// ------------------------------------------------------------ mbarrier + bulk copy
+// Shared-memory barriers with transaction counts and the non-tensor bulk
+// copy engine (TMA): one thread moves a whole FIFO slot or input slice
+// into shared memory and the barrier completes when the bytes have landed.
+
+__device__ __forceinline__ uint32_t smemAddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbarInit(unsigned long long* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smemAddr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbarExpectTx(unsigned long long* bar, unsigned bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smemAddr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbarArrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smemAddr(bar)) : "memory");
+}
+// true once the phase of the given parity has completed
+__device__ __forceinline__ bool mbarTryWait(unsigned long long* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smemAddr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// global -> shared bulk copy; bytes and both addresses multiples of 16
+__device__ __forceinline__ void bulkLoad(void* dstSmem, const void* srcGlobal, unsigned bytes,
+                                         unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smemAddr(dstSmem)),
+      "l"(srcGlobal), "r"(bytes), "r"(smemAddr(bar))
+      : "memory");
+}
+// Starts pulling a global range into L2 (no destination in this SM).
+__device__ __forceinline__ void bulkPrefetchL2(const void* srcGlobal, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(srcGlobal), "r"(bytes) : "memory");
+}
+// Orders this thread's earlier generic-proxy accesses (the flag acquire)
+// before its later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fenceProxyAsync() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned atomAddAcqRelCta(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smemAddr(p)), "r"(v)
+               : "memory");
+  return old;
+}
+// Drops a 128-byte L2 line without writing it back: for a FIFO slot whose
+// contents have been consumed and will be rewritten by its sender.
+__device__ __forceinline__ void discardL2(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+__device__ __forceinline__ void redMaxRelaxed(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // ------------------------------------------------------------ bounded waits
 
 // Records the first failure of the launch and raises the device abort word.
@@ -82,24 +146,33 @@ __device__ __forceinline__ void recordFailure(const DevComm& c, int code, int ra
   atomicExch(c.devAbort, 1);
 }
 
-// One spinning thread's budget: every 1024 polls it checks the abort words
-// and the clock; past the communicator's timeout it records vrcclTimeout.
+// One spinning thread's budget. Every `mask+1` polls it reads the clock;
+// the abort words (one of them in host memory, a slow read) and the
+// timeout are checked only when at least kCheckNs have passed since the last
+// check, so a waiter is rarely stuck in a slow read when its flag arrives.
+// Past the communicator's timeout it records vrcclTimeout.
 struct Spin {
-  unsigned long long t0;
+  static constexpr unsigned long long kCheckNs = 50000;
+  unsigned long long t0, last;
   unsigned n;
-  __device__ __forceinline__ Spin() : t0(0), n(0) {}
+  unsigned mask;
+  __device__ __forceinline__ Spin(unsigned mask_ = 255u) : t0(0), last(0), n(0), mask(mask_) {}
   // true = give up
   __device__ __forceinline__ bool tick(const DevComm& c, int rank, int ch, int kind, unsigned long long step) {
-    if ((++n & 1023u) != 0) return false;
+    if ((++n & mask) != 0) return false;
+    const unsigned long long now = globalTimer();
+    if (t0 == 0) {
+      t0 = last = now;
+      return false;
+    }
+    if (now - last < kCheckNs) return false;
+    last = now;
     if (*reinterpret_cast<volatile int*>(c.devAbort)) return true;
     if (*c.hostAbort) {
       recordFailure(c, vrcclAborted, rank, ch, kind, step);
       return true;
     }
-    unsigned long long now = globalTimer();
-    if (t0 == 0) {
-      t0 = now;
-    } else if (now - t0 > c.timeoutNs) {
+    if (now - t0 > c.timeoutNs) {
       recordFailure(c, vrcclTimeout, rank, ch, kind, step);
       return true;
     }

@@ -155,61 +155,6 @@ __device__ __forceinline__ typename Ty<DT>::S reduceElem(typename Ty<DT>::S x, t
   return v;
 }
 
-// ------------------------------------------------------------------ Simple
-// One slice = one slot of raw elements. Data moves in 16-byte vectors; the
-// ragged end (fewer than 16 bytes at the very end of the user buffer) goes
-// element by element. After the CTA barrier one thread makes the CTA's
-// stores visible at gpu scope (the fence is cumulative over the barrier)
-// and then publishes the new tail / head.
-template <int DT, int OP, bool TREE>
-__device__ bool simpleSlice(const KArgs& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
-  using S = typename Ty<DT>::S;
-  constexpr int V = 16 / sizeof(S);
-  __shared__ int smFail;
-  const DevComm& c = a.comm;
-  if (!slicePrologue(c, ag, flags, true, &smFail)) return false;
-
-  const char* src0 = (flags & F_RECV) && ag.nrecv > 0 ? ag.slot(c, ag.re[0], ag.rstep[0]) : nullptr;
-  const char* src1 = (flags & F_RECV) && ag.nrecv > 1 ? ag.slot(c, ag.re[1], ag.rstep[1]) : nullptr;
-  char* dst0 = (flags & F_SEND) && ag.nsend > 0 ? ag.slot(c, ag.se[0], ag.sstep[0]) : nullptr;
-  char* dst1 = (flags & F_SEND) && ag.nsend > 1 ? ag.slot(c, ag.se[1], ag.sstep[1]) : nullptr;
-
-  const int nv = nelem / V;
-  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-    const size_t b = size_t(i) * 16;
-    uint4 xv = make_uint4(0, 0, 0, 0), r0v = xv, r1v = xv;
-    if (flags & F_IN) xv = ldStream16(in + b);
-    if (src0) r0v = ldFifo16(src0 + b);
-    if (src1) r1v = ldFifo16(src1 + b);
-    uint32_t x[4] = {xv.x, xv.y, xv.z, xv.w}, r0[4] = {r0v.x, r0v.y, r0v.z, r0v.w},
-             r1[4] = {r1v.x, r1v.y, r1v.z, r1v.w}, acc[4];
-    reduceWords<DT, OP, TREE, 4>(acc, x, r0, r1, flags, ag.nrecv, a.scale, a.nranks);
-    uint4 av = make_uint4(acc[0], acc[1], acc[2], acc[3]);
-    if (dst0) stFifo16(dst0 + b, av);
-    if (dst1) stFifo16(dst1 + b, av);
-    if (flags & F_OUT) stStream16(out + b, av);
-  }
-  for (int j = nv * V + threadIdx.x; j < nelem; j += blockDim.x) {
-    S x = (flags & F_IN) ? reinterpret_cast<const S*>(in)[j] : S(0);
-    S r0 = src0 ? __ldcg(reinterpret_cast<const S*>(src0) + j) : S(0);
-    S r1 = src1 ? __ldcg(reinterpret_cast<const S*>(src1) + j) : S(0);
-    S v = reduceElem<DT, OP, TREE>(x, r0, r1, flags, ag.nrecv, a.scale, a.nranks);
-    if (dst0) reinterpret_cast<S*>(dst0)[j] = v;
-    if (dst1) reinterpret_cast<S*>(dst1)[j] = v;
-    if (flags & F_OUT) reinterpret_cast<S*>(out)[j] = v;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    fenceAcqRelGpu();
-    if (flags & F_SEND)
-      for (int i = 0; i < ag.nsend; ++i) stRelaxed(&c.ctrl[kSimple][ag.se[i]].tail, ag.sstep[i] + 1);
-    if (flags & F_RECV)
-      for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[kSimple][ag.re[i]].head, ag.rstep[i] + 1);
-  }
-  ag.advance(flags);
-  return true;
-}
-
 // ------------------------------------------------------- 8-byte user units
 // LL and LL128 carry user data in 8-byte units. The last unit of a user
 // buffer may be partial: read and write only its valid elements.
@@ -431,7 +376,6 @@ __device__ bool llSlice128(const KArgs& a, Agent& ag, const char* in, char* out,
 template <int PROTO, int DT, int OP, bool TREE>
 __device__ __forceinline__ bool runSlice(const KArgs& a, Agent& ag, const char* in, char* out, int nelem,
                                          int flags) {
-  if constexpr (PROTO == kSimple) return simpleSlice<DT, OP, TREE>(a, ag, in, out, nelem, flags);
   if constexpr (PROTO == kLL) return llSlice<DT, OP, TREE>(a, ag, in, out, nelem, flags);
   if constexpr (PROTO == kLL128) return llSlice128<DT, OP, TREE>(a, ag, in, out, nelem, flags);
 }

@@ -2,7 +2,7 @@
 // co-resident (cooperative launch), so every wait is on a running peer.
 #pragma once
 
-#include "engine.cuh"
+#include "simple_pipe.cuh"
 
 namespace vrccl {
 
@@ -38,7 +38,6 @@ __device__ __forceinline__ void channelRange(unsigned long long count, int C, in
 template <int PROTO, int DT, int OP>
 __global__ void __launch_bounds__(1024) ringKernel(const __grid_constant__ KArgs a) {
   using S = typename Ty<DT>::S;
-  constexpr long long A = 16 / sizeof(S);
   constexpr long long E = sizeof(S);
   const int n = a.nranks;
   const int r = blockIdx.x % n, ch = blockIdx.x / n;
@@ -46,55 +45,25 @@ __global__ void __launch_bounds__(1024) ringKernel(const __grid_constant__ KArgs
   if (aborted(c)) return;
   unsigned long long lo, hi;
   channelRange<S>(a.count, a.nchannels, ch, lo, hi);
-  const long long chCount = (long long)(hi - lo);
   const char* in = reinterpret_cast<const char*>(a.send[r]) + lo * E;
   char* out = reinterpret_cast<char*>(a.recv[r]) + lo * E;
-  const long long slice = a.sliceElems;
 
   Agent ag;
   ag.init(c, PROTO, r, ch);
-  if (n == 1) {  // single rank: a local copy through the same arithmetic
-    for (long long s = 0; s < chCount; s += slice) {
-      const int m = (int)min(slice, chCount - s);
-      if (!runSlice<PROTO, DT, OP, false>(a, ag, in + s * E, out + s * E, m, F_IN | F_OUT | F_POST)) return;
-    }
-    return;
+  if (n > 1) {
+    ag.addRecv(c, ringEdge(ch, (r - 1 + n) % n, n));
+    ag.addSend(c, ringEdge(ch, r, n));
   }
-  ag.addRecv(c, ringEdge(ch, (r - 1 + n) % n, n));
-  ag.addSend(c, ringEdge(ch, r, n));
-
-  const long long K = a.chunkElems;
-  const long long loop = (long long)n * K;
-  for (long long off = 0; off < chCount; off += loop) {
-    const long long rem = chCount - off;
-    const long long k = rem >= loop ? K : ((rem + n - 1) / n + A - 1) / A * A;
-    for (int p = 0; p < 2 * n - 1; ++p) {
-      int cidx, flags;
-      if (p == 0) {
-        cidx = (r - 1 + n) % n;
-        flags = F_IN | F_SEND;
-      } else if (p <= n - 2) {
-        cidx = ((r - 1 - p) % n + n) % n;
-        flags = F_IN | F_RECV | F_SEND;
-      } else if (p == n - 1) {
-        cidx = r;
-        flags = F_IN | F_RECV | F_POST | F_OUT | F_SEND;
-      } else if (p <= 2 * n - 3) {
-        cidx = ((r - (p - n + 1)) % n + n) % n;
-        flags = F_RECV | F_OUT | F_SEND;
-      } else {
-        cidx = (r + 1) % n;
-        flags = F_RECV | F_OUT;
-      }
-      const long long cLo = min(rem, (long long)cidx * k), cHi = min(rem, (long long)(cidx + 1) * k);
-      for (long long s = cLo; s < cHi; s += slice) {
-        const int m = (int)min(slice, cHi - s);
-        const long long pos = off + s;
-        if (!runSlice<PROTO, DT, OP, false>(a, ag, in + pos * E, out + pos * E, m, flags)) return;
-      }
-    }
+  RingIter it;
+  it.init(n, r, (long long)(hi - lo), a.chunkElems, 16 / E, a.sliceElems);
+  if constexpr (PROTO == kSimple) {
+    simplePipeline<DT, OP, false>(a, ag, it, in, out);
+  } else {
+    SliceDesc d;
+    while (it.next(d))
+      if (!runSlice<PROTO, DT, OP, false>(a, ag, in + d.pos * E, out + d.pos * E, d.nelem, d.flags)) return;
+    ag.finish(c);
   }
-  ag.finish(c);
 }
 
 // ---------------------------------------------------------------------- tree
@@ -203,15 +172,18 @@ __global__ void __launch_bounds__(1024) treeKernel(const __grid_constant__ KArgs
 
   unsigned long long lo, hi;
   channelRange<S>(a.count, a.nchannels, ch, lo, hi);
-  const long long chCount = (long long)(hi - lo);
   const char* in = reinterpret_cast<const char*>(a.send[rank]) + lo * E;
   char* out = reinterpret_cast<char*>(a.recv[rank]) + lo * E;
-  const long long slice = a.sliceElems;
-  for (long long s = 0; s < chCount; s += slice) {
-    const int m = (int)min(slice, chCount - s);
-    if (!runSlice<PROTO, DT, OP, true>(a, ag, in + s * E, out + s * E, m, flags)) return;
+  TreeIter it;
+  it.init((long long)(hi - lo), a.sliceElems, flags);
+  if constexpr (PROTO == kSimple) {
+    simplePipeline<DT, OP, true>(a, ag, it, in, out);
+  } else {
+    SliceDesc d;
+    while (it.next(d))
+      if (!runSlice<PROTO, DT, OP, true>(a, ag, in + d.pos * E, out + d.pos * E, d.nelem, d.flags)) return;
+    ag.finish(c);
   }
-  ag.finish(c);
 }
 
 // Explicit instantiation of every (dtype, op) for one protocol, and its

@@ -1,0 +1,313 @@
+// Simple protocol as a warp-specialised pipeline.
+//
+// The Simple wire format is unchanged: a slot of raw elements, published by
+// raising the edge's tail counter once the whole slot is written, drained
+// by raising its head counter ("NCCL architecture: topology, channels,
+// algorithms and protocols", §6.5 and §7.2). What changes is how one agent
+// (CTA) moves its slices:
+//
+//   warp 0, one thread   input producer: as soon as stage q % S of the
+//                        shared-memory ring is free it bulk-copies (TMA,
+//                        cp.async.bulk) the agent's input slice q into it.
+//   warp 1, one thread   FIFO producer: waits until the out-edge slot of
+//                        slice q is drained and its in-edge slot filled
+//                        (cached flag values cover several slices per
+//                        poll), then bulk-copies the received slot(s) next to
+//                        the input.
+//   warp 2, one thread   publisher: once every consumer warp is past a run
+//                        of slices it publishes them with one gpu-scope fence
+//                        and the new tail (sent) and head (drained) counters.
+//   warps 3..W+2         consumers. They wait for the stage, reduce from
+//                        shared memory, store the result to the out-edge
+//                        slot and/or the recv buffer, free the stage and
+//                        report the slice done. They never fence at gpu
+//                        scope, so no consumer waits for the memory system.
+//
+// So the producer keeps up to S slices of input and FIFO data in flight
+// while consumers work, and no CTA-wide barrier is taken per slice.
+#pragma once
+
+#include "schedule.cuh"
+
+namespace vrccl {
+
+struct PipeShared {
+  unsigned long long fullIn[kMaxStages];    // input producer's copies landed
+  unsigned long long fullFifo[kMaxStages];  // FIFO producer's copies landed
+  unsigned long long empty[kMaxStages];
+  unsigned prog[kMaxConsumerWarps];  // slices finished by each consumer warp
+  int abort;
+};
+
+// Bounded wait on a shared-memory barrier phase; false = give up.
+__device__ __forceinline__ bool pipeWait(const DevComm& c, const Agent& ag, PipeShared* sh,
+                                         unsigned long long* bar, unsigned parity) {
+  Spin sp(15u);
+  while (!mbarTryWait(bar, parity)) {
+    if (*reinterpret_cast<volatile int*>(&sh->abort)) return false;
+    if (sp.tick(c, ag.rank, ag.ch, 4, 0)) return false;
+  }
+  return true;
+}
+
+// Producer side of a flag wait with a cached last-seen value.
+__device__ __forceinline__ bool flagAtLeast(const DevComm& c, const Agent& ag, const unsigned long long* p,
+                                            unsigned long long need, unsigned long long& seen, int kind) {
+  if (seen >= need) return true;
+  Spin sp;
+  unsigned long long v;
+  while ((v = ldAcquire(p)) < need) {
+    if (sp.tick(c, ag.rank, ag.ch, kind, need)) return false;
+  }
+  seen = v;
+  return true;
+}
+
+// Waits (bounded) until every bulk copy this thread issued into the stage
+// ring has landed; a CTA must not exit with copies into its shared memory in
+// flight.
+__device__ __forceinline__ void drainStages(const DevComm& c, unsigned long long* full, const int* lastUse,
+                                            int nst) {
+  for (int i = 0; i < nst; ++i) {
+    if (lastUse[i] < 0) continue;
+    const unsigned long long t0 = globalTimer();
+    while (!mbarTryWait(&full[i], lastUse[i] & 1)) {
+      if (globalTimer() - t0 > c.timeoutNs) break;
+    }
+  }
+}
+
+template <int DT, int OP, bool TREE, class It>
+__device__ void simplePipeline(const KArgs& a, Agent& ag, It it, const char* in, char* out) {
+  using S = typename Ty<DT>::S;
+  constexpr int E = sizeof(S);
+  constexpr int V = 16 / E;
+  constexpr int NBUF = TREE ? 3 : 2;  // own input + up to (NBUF-1) received slots
+  extern __shared__ __align__(128) char smemDyn[];
+  __shared__ PipeShared sh;
+  const DevComm& c = a.comm;
+  const int NST = a.stages;
+  const size_t sliceBytes = size_t(a.sliceElems) * E;
+  const int W = (blockDim.x >> 5) - 3;  // consumer warps
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbarInit(&sh.fullIn[i], 1);
+      mbarInit(&sh.fullFifo[i], 1);
+      mbarInit(&sh.empty[i], W);
+    }
+    for (int w = 0; w < W; ++w) sh.prog[w] = 0;
+    sh.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------- input producer
+    // Streams this agent's own input slices into the stage ring as soon as
+    // a stage is free; it never waits on another agent.
+    if (lane != 0) return;
+    int lastUse[kMaxStages];
+    for (int i = 0; i < NST; ++i) lastUse[i] = -1;
+    // A second walk of the same sequence, a.prefetch slices ahead, pulls
+    // future input slices into L2 so the stage copies hit L2, not HBM.
+    It ahead = it;
+    SliceDesc pd;
+    bool pmore = a.prefetch > 0;
+    for (int k = 0; k < a.prefetch && pmore; ++k) {
+      pmore = ahead.next(pd);
+      if (pmore && (pd.flags & F_IN) && pd.nelem * E >= 16) bulkPrefetchL2(in + pd.pos * E, unsigned(pd.nelem * E / 16 * 16));
+    }
+    SliceDesc d;
+    long long q = 0;
+    bool ok = true;
+    while (it.next(d)) {
+      const int st = (int)(q % NST);
+      const int use = (int)(q / NST);
+      if (pmore && (pmore = ahead.next(pd)) && (pd.flags & F_IN) && pd.nelem * E >= 16)
+        bulkPrefetchL2(in + pd.pos * E, unsigned(pd.nelem * E / 16 * 16));
+      if (!pipeWait(c, ag, &sh, &sh.empty[st], (use & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      const unsigned inBytes = (d.flags & F_IN) ? unsigned(d.nelem * E / 16 * 16) : 0u;
+      if (inBytes) {
+        lastUse[st] = use;
+        mbarExpectTx(&sh.fullIn[st], inBytes);
+        bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes, in + d.pos * E, inBytes, &sh.fullIn[st]);
+      }
+      mbarArrive(&sh.fullIn[st]);
+      ++q;
+    }
+    if (!ok) {
+      *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+      drainStages(c, sh.fullIn, lastUse, NST);
+    }
+    return;
+  }
+
+  if (warp == 1) {
+    // -------------------------------------------------- FIFO producer
+    // For each slice: wait until the out-edge slot is drained and the
+    // in-edge slot is filled (cached flag values cover several slices per
+    // poll), then bulk-copy the received slot(s) into the stage.
+    if (lane != 0) return;
+    unsigned long long headSeen[2] = {0, 0}, tailSeen[2] = {0, 0};
+    int lastUse[kMaxStages];
+    for (int i = 0; i < NST; ++i) lastUse[i] = -1;
+    SliceDesc d;
+    long long q = 0;
+    bool ok = true;
+    while (it.next(d)) {
+      const int st = (int)(q % NST);
+      const int use = (int)(q / NST);
+      if (ag.faultNow(c) || !pipeWait(c, ag, &sh, &sh.empty[st], (use & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      const unsigned rvBytes = unsigned((d.nelem * E + 15) / 16 * 16);
+      if (d.flags & F_SEND) {
+        for (int i = 0; i < ag.nsend && ok; ++i) {
+          const unsigned long long need = ag.sstep[i] + 1;
+          if (need > (unsigned long long)kSteps)
+            ok = flagAtLeast(c, ag, &c.ctrl[kSimple][ag.se[i]].head, need - kSteps, headSeen[i], 1);
+        }
+      }
+      if (ok && (d.flags & F_RECV)) {
+        char* buf = smemDyn + size_t(st) * NBUF * sliceBytes;
+        for (int i = 0; i < ag.nrecv && ok; ++i) {
+          const unsigned long long before = tailSeen[i];
+          ok = flagAtLeast(c, ag, &c.ctrl[kSimple][ag.re[i]].tail, ag.rstep[i] + 1, tailSeen[i], 0);
+          if (!ok) break;
+          if (tailSeen[i] != before) fenceProxyAsync();
+          lastUse[st] = use;
+          mbarExpectTx(&sh.fullFifo[st], rvBytes);
+          bulkLoad(buf + size_t(1 + i) * sliceBytes, ag.slot(c, ag.re[i], ag.rstep[i]), rvBytes, &sh.fullFifo[st]);
+        }
+      }
+      // On failure the consumers are told before this arrival, so the stage
+      // it may complete is never published.
+      if (!ok) *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+      mbarArrive(&sh.fullFifo[st]);
+      if (!ok) break;
+      ag.advance(d.flags);
+      ++q;
+    }
+    if (!ok) {
+      *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+      drainStages(c, sh.fullFifo, lastUse, NST);
+    }
+    return;
+  }
+
+  if (warp == 2) {
+    // ------------------------------------------------------- publisher
+    // Slices are complete once every consumer warp has moved past them.
+    // Whatever has completed since the last pass is published at once:
+    // one gpu-scope fence (cumulative over the consumers' stores, which the
+    // CTA-scope acquire below ordered before it), then the new tail of each
+    // out-edge and head of each in-edge.
+    if (lane != 0) return;
+    SliceDesc d;
+    long long q = 0;  // slices published so far
+    bool more = it.next(d);
+    Spin sp(15u);
+    while (more) {
+      unsigned done = 0xffffffffu;
+      for (int w = 0; w < W; ++w) {
+        unsigned v;
+        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smemAddr(&sh.prog[w])) : "memory");
+        done = min(done, v);
+      }
+      if ((long long)done <= q) {
+        if (*reinterpret_cast<volatile int*>(&sh.abort) || sp.tick(c, ag.rank, ag.ch, 4, 0)) return;
+        continue;
+      }
+      bool send = false, recv = false;
+      while (more && q < (long long)done) {
+        send |= (d.flags & F_SEND) != 0;
+        recv |= (d.flags & F_RECV) != 0;
+        ag.advance(d.flags);
+        ++q;
+        more = it.next(d);
+      }
+      if (send || recv) {
+        fenceAcqRelGpu();
+        if (send)
+          for (int i = 0; i < ag.nsend; ++i) redMaxRelaxed(&c.ctrl[kSimple][ag.se[i]].tail, ag.sstep[i]);
+        if (recv)
+          for (int i = 0; i < ag.nrecv; ++i) redMaxRelaxed(&c.ctrl[kSimple][ag.re[i]].head, ag.rstep[i]);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int ct = threadIdx.x - 96, CT = W * 32;
+  const int cw = warp - 3;
+  SliceDesc d;
+  long long q = 0;
+  while (it.next(d)) {
+    const int st = (int)(q % NST);
+    const int use = (int)(q / NST);
+    if (!pipeWait(c, ag, &sh, &sh.fullIn[st], use & 1)) return;
+    if (!pipeWait(c, ag, &sh, &sh.fullFifo[st], use & 1)) return;
+    if (*reinterpret_cast<volatile int*>(&sh.abort)) return;
+    const char* buf = smemDyn + size_t(st) * NBUF * sliceBytes;
+    const char* sIn = buf;
+    const char* sR0 = buf + sliceBytes;
+    const char* sR1 = buf + 2 * sliceBytes;
+    const bool rv = (d.flags & F_RECV) && ag.nrecv > 0;
+    char* dst0 = (d.flags & F_SEND) && ag.nsend > 0 ? ag.slot(c, ag.se[0], ag.sstep[0]) : nullptr;
+    char* dst1 = (d.flags & F_SEND) && ag.nsend > 1 ? ag.slot(c, ag.se[1], ag.sstep[1]) : nullptr;
+    char* o = out + d.pos * E;
+    const int nv = d.nelem / V;
+    for (int i = ct; i < nv; i += CT) {
+      const size_t b = size_t(i) * 16;
+      uint4 xv = make_uint4(0, 0, 0, 0), r0v = xv, r1v = xv;
+      if (d.flags & F_IN) xv = *reinterpret_cast<const uint4*>(sIn + b);
+      if (rv) r0v = *reinterpret_cast<const uint4*>(sR0 + b);
+      if (rv && ag.nrecv > 1) r1v = *reinterpret_cast<const uint4*>(sR1 + b);
+      uint32_t x[4] = {xv.x, xv.y, xv.z, xv.w}, r0[4] = {r0v.x, r0v.y, r0v.z, r0v.w},
+               r1[4] = {r1v.x, r1v.y, r1v.z, r1v.w}, acc[4];
+      reduceWords<DT, OP, TREE, 4>(acc, x, r0, r1, d.flags, ag.nrecv, a.scale, a.nranks);
+      const uint4 av = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+      if (dst0) stFifo16(dst0 + b, av);
+      if (dst1) stFifo16(dst1 + b, av);
+      if (d.flags & F_OUT) stStream16(o + b, av);
+    }
+    for (int j = nv * V + ct; j < d.nelem; j += CT) {  // ragged end of the user buffer
+      S x = (d.flags & F_IN) ? reinterpret_cast<const S*>(in + d.pos * E)[j] : S(0);
+      S r0 = rv ? reinterpret_cast<const S*>(sR0)[j] : S(0);
+      S r1 = (rv && ag.nrecv > 1) ? reinterpret_cast<const S*>(sR1)[j] : S(0);
+      S v = reduceElem<DT, OP, TREE>(x, r0, r1, d.flags, ag.nrecv, a.scale, a.nranks);
+      if (dst0) reinterpret_cast<S*>(dst0)[j] = v;
+      if (dst1) reinterpret_cast<S*>(dst1)[j] = v;
+      if (d.flags & F_OUT) reinterpret_cast<S*>(o)[j] = v;
+    }
+    if (rv) {
+      // The received slot(s) now sit in shared memory and the sender will
+      // rewrite them: drop their L2 lines instead of letting them be written
+      // back to HBM. The report below orders this before the head that
+      // lets the sender reuse the slot.
+      const int lines = (d.nelem * E + 127) / 128;
+      for (int i = 0; i < ag.nrecv; ++i) {
+        const char* slotp = ag.slot(c, ag.re[i], ag.rstep[i]);
+        for (int l = ct; l < lines; l += CT) discardL2(slotp + size_t(l) * 128);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      // Free the stage (its shared memory has been read), then report the
+      // slice done; the release orders this warp's stores before the report.
+      mbarArrive(&sh.empty[st]);
+      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smemAddr(&sh.prog[cw])), "r"(unsigned(q + 1))
+                   : "memory");
+    }
+    ag.advance(d.flags);
+    ++q;
+  }
+}
+
+}  // namespace vrccl

@@ -66,6 +66,8 @@ struct vrcclComm {
   int forceChannels;
   size_t forceChunkBytes;
   int envProto, envAlgo, envChannels;
+  size_t envSliceBytes;
+  int envWarps, envPrefetch;
   bool debug;
   bool haveLast;
   int lastAlgo, lastProto, lastChannels;
@@ -195,6 +197,9 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
   c->envProto = parseProto(getenv("VRCCL_PROTO"));
   c->envAlgo = parseAlgo(getenv("VRCCL_ALGO"));
   c->envChannels = std::min(envInt("VRCCL_NCHANNELS", 0), nchannels);
+  c->envSliceBytes = (size_t)std::max(0, envInt("VRCCL_SLICE_BYTES", 0)) / 16 * 16;
+  c->envWarps = std::max(0, envInt("VRCCL_SIMPLE_WARPS", 0));
+  c->envPrefetch = std::min(kMaxPrefetch, std::max(0, envInt("VRCCL_PREFETCH", 0)));
   c->tuner.loadEnvFile(nranks);
   *comm = c;
   return vrcclSuccess;
@@ -298,20 +303,67 @@ extern "C" vrcclResult_t vrcclCommGetLastSchedule(vrcclComm_t comm, int* algo, i
 
 // ------------------------------------------------------------------ launch
 
-// Blocks of `threads` threads of `fn` that can be resident at once.
-static int residentCapacity(const vrcclComm* c, const void* fn, int threads) {
+// Blocks of `threads` threads of `fn` with `smem` bytes of dynamic shared
+// memory that can be resident at once on the device.
+static int residentCapacity(const vrcclComm* c, const void* fn, int threads, size_t smem) {
+  struct Key {
+    const void* fn;
+    int threads;
+    size_t smem;
+    int per;
+  };
   static std::mutex mu;
-  static std::vector<std::pair<std::pair<const void*, int>, int>> cache;
+  static std::vector<Key> cache;
   std::lock_guard<std::mutex> lk(mu);
   for (auto& e : cache)
-    if (e.first.first == fn && e.first.second == threads) return e.second * c->smCount;
+    if (e.fn == fn && e.threads == threads && e.smem == smem) return e.per * c->smCount;
+  if (smem > 0) {
+    static std::vector<const void*> raised;
+    if (std::find(raised.begin(), raised.end(), fn) == raised.end()) {
+      int optin = 0;
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+      cudaGetLastError();
+      raised.push_back(fn);
+    }
+  }
   int per = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, threads, 0) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, threads, smem) != cudaSuccess) {
     cudaGetLastError();
     per = 0;
   }
-  cache.push_back({{fn, threads}, per});
+  cache.push_back({fn, threads, smem, per});
   return per * c->smCount;
+}
+
+// Shape of one Simple agent: 2 producer warps, a publisher warp and W
+// consumer warps, `stages`
+// shared-memory stages of (own input + received slots) x slice bytes. The
+// first shape (most consumer warps, deepest pipeline, largest slice) with
+// which every agent of the launch is resident at once wins.
+struct SimpleShape {
+  int threads;
+  int stages;
+  size_t sliceBytes;
+  size_t smem;
+};
+static bool pickSimpleShape(const vrcclComm* c, const void* fn, int agents, int nbuf, size_t maxSlice,
+                            int maxWarps, SimpleShape* out) {
+  static const int kWarps[] = {16, 8, 4, 2, 1};
+  for (size_t slice = maxSlice; slice >= 2048; slice /= 2) {
+    for (int st = kMaxStages; st >= 2; --st) {
+      for (int w : kWarps) {
+        if (w > maxWarps) continue;
+        const size_t smem = size_t(st) * nbuf * slice;
+        const int threads = 32 * (3 + w);
+        if (residentCapacity(c, fn, threads, smem) >= agents) {
+          *out = {threads, st, slice, smem};
+          return true;
+        }
+      }
+    }
+  }
+  return false;
 }
 
 static int agentsPerChannel(int algo, int n) { return algo == kRing ? n : 2 * n - 1; }
@@ -369,30 +421,54 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
 
   const void* fn = kernelFor(A, P, dtype, op);
   if (!fn) return vrcclInternalError;
-  int threads = P == kSimple ? 512 : 256;
   const int per = agentsPerChannel(A, n);
-  // All agents of a launch wait on each other: they must all be resident.
-  // Shrink the CTA first, then (if the caller left it open) the channels.
-  int cap = residentCapacity(comm, fn, threads);
-  while (cap < per * C && threads > 64) {
-    threads /= 2;
-    cap = residentCapacity(comm, fn, threads);
+  if (!userChannels && ch.channels == 0 && per * C > comm->smCount) {
+    // Every agent does the same work, so a launch runs at the pace of the
+    // most crowded SM: use a whole number of agents per SM.
+    const int k = per * C / comm->smCount;
+    C = std::max(1, k * comm->smCount / per);
   }
-  if (cap < per * C) {
-    if (userChannels) return vrcclInvalidUsage;
-    C = cap / per;
-    if (C < 1) return userAlgo ? vrcclInvalidUsage : vrcclInternalError;
+  int threads = 256, stages = 0;
+  size_t smem = 0;
+  size_t sliceBytes = slotDataBytes(P);
+  if (P == kSimple) {
+    // All agents of a launch wait on each other: they must all be resident.
+    // Shrink the agent first, then (if the caller left it open) the channels.
+    const int nbuf = A == kTree ? 3 : 2;
+    const size_t want = std::min(comm->envSliceBytes ? comm->envSliceBytes
+                                 : ch.sliceBytes     ? ch.sliceBytes
+                                                     : kSimpleSlotBytes,
+                                 kSimpleSlotBytes);
+    SimpleShape sh;
+    const int maxWarps = comm->envWarps ? comm->envWarps : 8;
+    while (!pickSimpleShape(comm, fn, per * C, nbuf, want, maxWarps, &sh)) {
+      if (userChannels || C == 1) return userAlgo || userChannels ? vrcclInvalidUsage : vrcclInternalError;
+      --C;
+    }
+    threads = sh.threads;
+    stages = sh.stages;
+    smem = sh.smem;
+    sliceBytes = sh.sliceBytes;
+  } else {
+    int cap = residentCapacity(comm, fn, threads, 0);
+    while (cap < per * C && threads > 64) {
+      threads /= 2;
+      cap = residentCapacity(comm, fn, threads, 0);
+    }
+    if (cap < per * C) {
+      if (userChannels) return vrcclInvalidUsage;
+      C = cap / per;
+      if (C < 1) return userAlgo ? vrcclInvalidUsage : vrcclInternalError;
+    }
+    if (P == kLL128) sliceBytes = sliceBytes / 240 * 240;  // whole lines and 16-byte slice starts
   }
-
-  // Slice: one FIFO slot. Chunk: VRCCL_STEPS/2 slots (ALLREDUCE_CHUNKSTEPS =
-  // NCCL_STEPS/2, Deep Dive (Japanese edition) ch.6); fewer slots than the
-  // FIFO depth per chunk is what keeps the credit ring deadlock-free.
-  size_t sliceBytes = P == kSimple ? (ch.sliceBytes ? ch.sliceBytes : size_t(32) * 1024) : slotDataBytes(P);
-  sliceBytes = std::min(sliceBytes, slotDataBytes(P));
-  if (P == kLL128) sliceBytes = sliceBytes / 240 * 240;  // whole lines and 16-byte slice starts
   sliceBytes = std::max<size_t>(sliceBytes / 16 * 16, 16);
   const int sliceElems = (int)(sliceBytes / E);
-  size_t chunkBytes = comm->forceChunkBytes ? comm->forceChunkBytes : (ch.chunkBytes ? ch.chunkBytes : sliceBytes * (kSteps / 2));
+  // Chunk: VRCCL_STEPS/2 slots (ALLREDUCE_CHUNKSTEPS = NCCL_STEPS/2, Deep
+  // Dive (Japanese edition) ch.6). Fewer slots per chunk than the FIFO depth
+  // is what keeps the credit ring deadlock-free.
+  size_t chunkBytes = comm->forceChunkBytes ? comm->forceChunkBytes
+                    : (ch.chunkBytes ? ch.chunkBytes : sliceBytes * (kSteps / 2));
   chunkBytes = std::min(chunkBytes, sliceBytes * (kSteps / 2));
   chunkBytes = std::max<size_t>(chunkBytes / 16 * 16, 16);
   const int chunkElems = (int)(chunkBytes / E);
@@ -422,6 +498,8 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
   ka.chunkElems = chunkElems;
   ka.sliceElems = sliceElems;
   ka.scale = 1.0f / (float)n;
+  ka.stages = stages;
+  ka.prefetch = P == kSimple ? comm->envPrefetch : 0;
   for (int r = 0; r < n; ++r) {
     ka.send[r] = sendbufs[r];
     ka.recv[r] = recvbufs[r];
@@ -430,6 +508,7 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)(per * C));
   cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

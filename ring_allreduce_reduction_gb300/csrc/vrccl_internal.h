@@ -42,10 +42,13 @@ enum ProtoId { kSimple = 0, kLL = 1, kLL128 = 2 };
 enum AlgoId { kRing = 0, kTree = 1 };
 
 // FIFO geometry (buffer bytes per slot) and the data one slot carries.
-constexpr size_t kSimpleSlotBytes = 64 * 1024;  // data bytes per Simple slot (max slice)
-constexpr int kLLSlotLines = 2048;              // 16-byte lines: 8 data bytes each
-constexpr int kLL128SlotLines = 512;            // 128-byte lines: 120 data bytes each
+constexpr size_t kSimpleSlotBytes = 32 * 1024;  // data bytes per Simple slot (max slice)
+constexpr int kLLSlotLines = 1024;              // 16-byte lines: 8 data bytes each
+constexpr int kLL128SlotLines = 256;            // 128-byte lines: 120 data bytes each
 constexpr int kLL128DataBytes = 120;
+constexpr int kMaxStages = 8;          // Simple pipeline depth in shared memory
+constexpr int kMaxConsumerWarps = 29;  // Simple: 3 service warps + up to 29 consumer warps
+constexpr int kMaxPrefetch = 32;       // Simple: largest input L2 prefetch distance (slices)
 
 __host__ __device__ constexpr size_t slotBufferBytes(int proto) {
   return proto == kSimple ? kSimpleSlotBytes
@@ -70,7 +73,7 @@ struct DevStatus {
   int code;  // vrcclResult_t of the first failure, 0 = none
   int rank;
   int channel;
-  int kind;  // 0 = tail wait, 1 = head wait, 2 = LL line, 3 = LL128 flag
+  int kind;  // 0 = tail wait, 1 = head wait, 2 = LL line, 3 = LL128 flag, 4 = stage barrier
   unsigned long long step;
 };
 
@@ -96,7 +99,8 @@ struct KArgs {
   int chunkElems;  // ring chunk K (elements, multiple of 16 bytes)
   int sliceElems;  // elements per FIFO step (one slot)
   float scale;     // avg pre-scale 1.0f / n (binary32)
-  int pad;
+  int stages;      // Simple: shared-memory stages of the slice pipeline
+  int prefetch;    // Simple: input slices pulled into L2 ahead of their stage (0 = off)
   const void* send[kMaxRanks];
   void* recv[kMaxRanks];
 };
