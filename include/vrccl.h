@@ -273,6 +273,37 @@ vrcclResult_t vrcclCommGetLaunchShape(vrcclComm_t comm, int* blocks, int* thread
  */
 vrcclResult_t vrcclCommLoadTuning(vrcclComm_t comm, const char* path, int* loaded);
 
+/*
+ * vrcclAllReduceNoAlloc -- the ring / Simple AllReduce of vrcclAllReduce,
+ * for callers that cannot allocate device memory when they need it (code
+ * running under a memory-pool manager that owns all of the device's
+ * memory, or a latency-critical path that cannot take cudaMalloc's implicit
+ * device synchronisation) and keep no communicator. The pages have no
+ * counterpart: NCCL always reduces through a communicator's buffers.
+ *   sendbufs, recvbufs, count, dtype, op, stream: as for vrcclAllReduce
+ *             (caller-owned, 16-byte aligned device buffers; in place
+ *             allowed).
+ *   nranks    1..32 virtual ranks (the count of sendbufs / recvbufs).
+ * Schedule: ring, Simple, min(4, 32 / nranks) channels, chunk 256 KiB
+ * (= vrcclCommSetSchedule(comm, that many channels, 262144) on the
+ * communicator path, with identical results).
+ * Memory: allocates nothing. Its scratch (FIFO slots, counters, status;
+ * about 16 MiB) is one static device array that every GPU loading the
+ * library holds until the process exits. The first call on a device looks
+ * up that array's address and prepares the kernels; make that first call
+ * before any stream capture. Every call then zeroes the counters and
+ * status words on `stream` and launches one kernel; calls share the
+ * array, so calls that overlap on the GPU (other streams, other host
+ * threads) race and give undefined results -- order them.
+ * Errors: vrcclInvalidArgument (null/misaligned pointers, bad enum,
+ * nranks < 1); vrcclInvalidUsage (nranks > 32: the scratch is too small --
+ * use a communicator); vrcclCudaError / vrcclInternalError (set-up or
+ * launch failed). Device-side failures are not reported (there is no
+ * communicator to ask); waits still give up after 2 s.
+ */
+vrcclResult_t vrcclAllReduceNoAlloc(const void* const* sendbufs, void* const* recvbufs, size_t count, int nranks,
+                                    vrcclDataType_t dtype, vrcclRedOp_t op, vrcclStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

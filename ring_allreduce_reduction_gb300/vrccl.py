@@ -54,6 +54,8 @@ _sig = {
     "vrcclCommInjectFault": [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int],
     "vrcclCommGetLaunchShape": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p],
     "vrcclCommLoadTuning": [ctypes.c_void_p, ctypes.c_char_p, _c_int_p],
+    "vrcclAllReduceNoAlloc": [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
+                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p],
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -118,6 +120,14 @@ def vrcclAllReduce(sendbufs, recvbufs, count: int, dtype, op, algo="ring", proto
     _check(_lib.vrcclAllReduce(S, R, count, _enum(DTYPES, dtype, "dtype"), _enum(OPS, op, "op"),
                                _enum(ALGOS, algo, "algo"), _enum(PROTOS, proto, "proto"), comm,
                                _stream(stream)), "vrcclAllReduce")
+
+
+def vrcclAllReduceNoAlloc(sendbufs, recvbufs, count: int, nranks: int, dtype, op, stream=None) -> None:
+    """The allocation-free ring/Simple AllReduce (see include/vrccl.h)."""
+    S = (ctypes.c_void_p * len(sendbufs))(*[_ptr(b) for b in sendbufs])
+    R = (ctypes.c_void_p * len(recvbufs))(*[_ptr(b) for b in recvbufs])
+    _check(_lib.vrcclAllReduceNoAlloc(S, R, count, nranks, _enum(DTYPES, dtype, "dtype"), _enum(OPS, op, "op"),
+                                      _stream(stream)), "vrcclAllReduceNoAlloc")
 
 
 def vrcclCommSetSchedule(comm, nchannels: int = 0, chunkBytes: int = 0) -> None:
