@@ -56,12 +56,65 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest value of x over all ranks of the process group (x itself
+    without one): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Every GPU runs its own, differently seeded problem (weak scaling)."""
+    return 1000 + rank
+
+
 def busbw_gbs(bytes_per_rank: int, n: int, seconds: float) -> float:
     """busbw = algbw * 2(n-1)/n with algbw = S / t ("NCCL architecture ...",
     introduction: the ring moves 2(n-1)/n * S per rank)."""
     if n == 1:
         return bytes_per_rank / seconds / 1e9
     return bytes_per_rank / seconds * 2 * (n - 1) / n / 1e9
+
+
+KERNEL_SOURCES = os.path.join(ROOT, "ring_allreduce_reduction_gb300", "csrc")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ring_simple_n8_fp32_256MiB.md")
+
+
+def kernel_sources_sha256() -> str:
+    """Hash of the library sources: ties an ncu summary to the kernel it measured."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(KERNEL_SOURCES)):
+        if f.endswith((".cu", ".cuh", ".h", ".cc")):
+            with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(bytes_per_rank: int):
+    """DRAM bytes per launch from the committed ncu summary, if it measured
+    the current kernel sources (else None). The summary holds lines
+    `kernel_sources_sha256: <hex>` and `dram_bytes_per_launch_<bytes>: <n>`."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            txt = f.read()
+    except OSError:
+        return None
+    kv = {}
+    for ln in txt.splitlines():
+        ln = ln.strip().strip("`")
+        if ":" in ln:
+            k, _, val = ln.partition(":")
+            kv[k.strip()] = val.strip()
+    if kv.get("kernel_sources_sha256") != kernel_sources_sha256():
+        return None
+    val = kv.get(f"dram_bytes_per_launch_{bytes_per_rank}")
+    return int(float(val)) if val else None
 
 
 def measured_peak():
@@ -129,31 +182,48 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(n: int, dtype: str, op: str, nch: int, chunk_elems: int, count: int) -> dict:
-    """The oracle as it stands, on a bounded sample of the workload."""
+def cpu_baseline(x: np.ndarray, dtype: str, op: str, nch: int, chunk_elems: int, min_seconds: float = 10.0) -> dict:
+    """The oracle as it stands on the bench's own inputs, replaying the
+    schedule the GPU ran (same channels and chunk), repeated until about
+    `min_seconds` of CPU time (at most 5 runs)."""
     from oracle import ring as oring
-    from ring_allreduce_reduction_gb300.workloads import make_inputs
-    x = make_inputs(n, count, dtype, "uniform", seed=0)
-    t0 = time.perf_counter()
-    oring.ring_allreduce(x, op, dtype, nch, chunk_elems)
-    dt = time.perf_counter() - t0
+    n, count = x.shape
+    times = []
+    while True:
+        t0 = time.perf_counter()
+        oring.ring_allreduce(x, op, dtype, nch, chunk_elems)
+        times.append(time.perf_counter() - t0)
+        if sum(times) >= min_seconds or len(times) >= 5:
+            break
+    dt = statistics.mean(times)
     S = count * ELEM[dtype]
     return {"value": round(busbw_gbs(S, n, dt), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"n={n} virtual ranks x {count} {dtype} ({S >> 20} MiB/rank), {nch} channel(s), "
-                      f"chunk {chunk_elems} elements, numpy step machine, single thread, {dt:.1f} s"}
+            "sample": f"the whole workload: n={n} x {count} {dtype} per rank ({S >> 20} MiB/rank), {nch} channels, "
+                      f"chunk {chunk_elems} elements; numpy step machine, one thread; {len(times)} run(s), "
+                      f"mean {dt:.2f} s"}
 
 
 def run_reference(args) -> int:
-    """Reference arm: the CPU oracle on host cores (rank 0 only)."""
+    """Reference arm: the CPU oracle on the host cores (rank 0 only). Each
+    step is a bounded sample of the workload (same n, dtype, op, ring order),
+    sized from a calibration run so the whole run takes about
+    args.ref_budget seconds."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     W = WORKLOAD
     n, dtype = W["nranks"], W["dtype"]
-    count = args.ref_count
-    nch, chunk = 1, 32768
     from oracle import ring as oring
     from ring_allreduce_reduction_gb300.workloads import make_inputs
+    nch, chunk = 1, 65536
+    probe = 1 << 20
+    xp = make_inputs(n, probe, dtype, "uniform", seed=0)
+    t0 = time.perf_counter()
+    oring.ring_allreduce(xp, W["op"], dtype, nch, chunk)
+    per_elem = (time.perf_counter() - t0) / probe
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    full = W["bytes_per_rank"] // ELEM[dtype]
+    count = int(min(full, max(1 << 16, per_step / max(per_elem, 1e-12)))) // 4 * 4
     x = make_inputs(n, count, dtype, "uniform", seed=0)
     for _ in range(args.warmup):
         oring.ring_allreduce(x, W["op"], dtype, nch, chunk)
@@ -162,17 +232,19 @@ def run_reference(args) -> int:
         t0 = time.perf_counter()
         oring.ring_allreduce(x, W["op"], dtype, nch, chunk)
         times.append(time.perf_counter() - t0)
-    t = max(times) if times else float("nan")
     S = count * ELEM[dtype]
-    v = busbw_gbs(S, n, statistics.mean(times))
+    mean = statistics.mean(times)
+    v = busbw_gbs(S, n, mean)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(times), 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * mean, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": W["name"] + f" (bounded sample: {S >> 20} MiB/rank)", "nranks": n,
-                   "bytes_per_rank": S, "op": W["op"], "algo": "ring", "channels": nch, "chunk_elems": chunk},
+        "config": {"workload": W["name"], "nranks": n, "bytes_per_rank": W["bytes_per_rank"],
+                   "sample_bytes_per_rank": S, "op": W["op"], "algo": "ring", "channels": nch,
+                   "chunk_elems": chunk},
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"n={n} x {count} {dtype} per rank, per step; worst step {t:.2f} s"},
+                         "sample": f"per step n={n} x {count} {dtype} per rank ({S >> 20} MiB/rank) of the "
+                                   f"{W['bytes_per_rank'] >> 20} MiB/rank workload; numpy step machine, one thread"},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -186,9 +258,11 @@ def main() -> int:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--cpu-count", type=int, default=1 << 22, help="elements per rank of the CPU sample")
-    ap.add_argument("--ref-count", type=int, default=1 << 21, help="elements per rank per reference step")
-    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=150.0, help="seconds the reference arm aims to take")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    ap.add_argument("--bytes-per-rank", type=int, default=0,
+                    help="profiling only: a smaller per-rank size than the workload's (reported in config)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -209,11 +283,14 @@ def main() -> int:
     from ring_allreduce_reduction_gb300 import vrccl as v
     from ring_allreduce_reduction_gb300.workloads import make_inputs
 
-    W = WORKLOAD
+    W = dict(WORKLOAD)
+    if args.bytes_per_rank:
+        W["bytes_per_rank"] = args.bytes_per_rank
+        W["name"] += f" (profiling size {args.bytes_per_rank} B/rank)"
     n, dtype = W["nranks"], W["dtype"]
     S = W["bytes_per_rank"]
     count = S // ELEM[dtype]
-    x = make_inputs(n, count, dtype, "uniform", seed=1000 + rank)
+    x = make_inputs(n, count, dtype, "uniform", seed=rank_seed(rank))
     send = torch.from_numpy(x).cuda()
     recv = torch.empty_like(send)
     sp, rp = [send[r] for r in range(n)], [recv[r] for r in range(n)]
@@ -254,10 +331,7 @@ def main() -> int:
     err = v.vrcclCommGetAsyncError(comm)
     if err:
         raise RuntimeError(f"device error in the timed region: {v.RESULTS[err]}")
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, "cuda")
     ms_step = total_ms / args.steps
     value = busbw_gbs(S, n, ms_step / 1e3) * world
 
@@ -266,38 +340,38 @@ def main() -> int:
     mean_kern_s = statistics.mean(kern_ms) / 1e3
     peak, peak_kind = measured_peak()
     achieved = algo_bytes / mean_kern_s / 1e9
+    traffic = profiled_traffic(S)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
                 "algorithmic_bytes_per_launch": algo_bytes}
 
     # ---- end to end through the public API with pinned host buffers
-    host_in = torch.from_numpy(x).pin_memory()
-    host_out = torch.empty_like(host_in).pin_memory()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        send.copy_(host_in, non_blocking=True)
-        step()
-        host_out.copy_(recv, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": round(busbw_gbs(S, n, e2e_ms / 1e3) * world, 3), "unit": "GB/s",
-           "h2d_bytes_per_step": n * S, "d2h_bytes_per_step": n * S, "ms_per_step": round(e2e_ms, 3)}
+    e2e = None
+    if not args.no_e2e:
+        host_in = torch.from_numpy(x).pin_memory()
+        host_out = torch.empty_like(host_in).pin_memory()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            send.copy_(host_in, non_blocking=True)
+            step()
+            host_out.copy_(recv, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        e2e_ms = max_over_ranks(e2e_ms, "cuda")
+        e2e = {"value": round(busbw_gbs(S, n, e2e_ms / 1e3) * world, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": n * S, "d2h_bytes_per_step": n * S, "ms_per_step": round(e2e_ms, 3)}
 
     v.vrcclCommDestroy(comm)
     if rank != 0:
         return 0
     cpu = None
     if not args.no_cpu:
-        cpu = cpu_baseline(n, dtype, W["op"], 1, sched["chunk_elems"], args.cpu_count)
+        cpu = cpu_baseline(x, dtype, W["op"], sched["nchannels"], sched["chunk_elems"])
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
