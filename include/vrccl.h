@@ -142,7 +142,8 @@ typedef enum {
  * at most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent,
  * default 8), VRCCL_PREFETCH (input slices a Simple agent pulls into L2
  * ahead of use, default 0 = off, at most 32), VRCCL_TUNE_FILE (a measured
- * tuning table, see vrcclCommLoadTuning).
+ * tuning table, see vrcclCommLoadTuning; without it the table shipped next
+ * to the library, tuning/gb300_n<nranks>.txt, is used when present).
  */
 vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchannels);
 

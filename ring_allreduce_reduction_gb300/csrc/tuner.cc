@@ -1,10 +1,13 @@
 #include "tuner.h"
 
+#include <dlfcn.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <string>
 
 #include "vrccl_internal.h"
 
@@ -26,20 +29,22 @@ static int log2Bucket(size_t bytes) {
   return b;
 }
 
-Choice Tuner::choose(int nranks, size_t bytes, int maxChannels) const {
-  Choice c{kRing, bytes <= 65536 ? kLL : bytes <= (size_t(2) << 20) ? kLL128 : kSimple, 0, 0, 0};
-  if (table_.empty()) return c;
+Choice Tuner::choose(int nranks, size_t bytes, int maxChannels, int algo, int proto) const {
+  Choice c{algo >= 0 ? algo : kRing,
+           proto >= 0 ? proto : (bytes <= 65536 ? kLL : bytes <= (size_t(2) << 20) ? kLL128 : kSimple), 0, 0, 0};
+  auto eligible = [&](const Entry& e) {
+    return e.nranks == nranks && e.channels <= maxChannels && (algo < 0 || e.algo == algo) &&
+           (proto < 0 || e.proto == proto);
+  };
   const int want = log2Bucket(bytes);
   int bestDist = 1 << 30;
   for (const Entry& e : table_)
-    if (e.nranks == nranks && e.channels <= maxChannels) bestDist = std::min(bestDist, std::abs(e.log2bytes - want));
+    if (eligible(e)) bestDist = std::min(bestDist, std::abs(e.log2bytes - want));
   if (bestDist == (1 << 30)) return c;
   double best = 1e300;
   for (const Entry& e : table_) {
-    if (e.nranks != nranks || e.channels > maxChannels || std::abs(e.log2bytes - want) != bestDist) continue;
-    // nearest measured size: pick the fastest there; ties keep the first
-    const int target = e.log2bytes;
-    (void)target;
+    // the nearest measured size; the fastest entry there (ties keep the first)
+    if (!eligible(e) || std::abs(e.log2bytes - want) != bestDist) continue;
     if (e.us < best) {
       best = e.us;
       c.algo = e.algo;
@@ -77,7 +82,16 @@ int Tuner::load(const char* path, int nranks) {
 
 void Tuner::loadEnvFile(int nranks) {
   const char* p = getenv("VRCCL_TUNE_FILE");
-  if (p && *p) load(p, nranks);
+  if (p && *p) {
+    load(p, nranks);
+    return;
+  }
+  Dl_info info;
+  if (dladdr(reinterpret_cast<const void*>(&defaultChannels), &info) == 0 || !info.dli_fname) return;
+  std::string dir(info.dli_fname);
+  const size_t slash = dir.rfind('/');
+  dir = slash == std::string::npos ? std::string(".") : dir.substr(0, slash);
+  load((dir + "/tuning/gb300_n" + std::to_string(nranks) + ".txt").c_str(), nranks);
 }
 
 }  // namespace vrccl

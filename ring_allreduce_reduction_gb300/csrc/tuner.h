@@ -38,10 +38,12 @@ class Tuner {
     size_t sliceBytes;
     double us;
   };
-  Choice choose(int nranks, size_t bytes, int maxChannels) const;
-  // Reads VRCCL_TUNE_FILE if set. Format: one entry per line,
-  // "nranks algo proto channels log2bytes sliceBytes microseconds";
-  // '#' starts a comment.
+  // algo / proto: -1 = free, else only entries with that value are eligible.
+  Choice choose(int nranks, size_t bytes, int maxChannels, int algo = -1, int proto = -1) const;
+  // Reads VRCCL_TUNE_FILE if set, else the table shipped next to the
+  // library (tuning/gb300_n<nranks>.txt) if there is one. Format: one entry
+  // per line, "nranks algo proto channels log2bytes sliceBytes
+  // microseconds"; '#' starts a comment.
   void loadEnvFile(int nranks);
   int load(const char* path, int nranks);  // entries read, -1 on error
   void add(const Entry& e) { table_.push_back(e); }

@@ -409,9 +409,10 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
   // ---- schedule: algo, proto, channels, chunk, slice, threads
   const size_t bytes = count * E;
   const bool userAlgo = algo != vrcclAlgoAuto, userProto = proto != vrcclProtoAuto;
-  Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels);
-  int A = userAlgo ? (int)algo : (comm->envAlgo >= 0 ? comm->envAlgo : ch.algo);
-  int P = userProto ? (int)proto : (comm->envProto >= 0 ? comm->envProto : ch.proto);
+  const int fixA = userAlgo ? (int)algo : comm->envAlgo, fixP = userProto ? (int)proto : comm->envProto;
+  Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, n == 1 ? kRing : fixA, fixP);
+  int A = fixA >= 0 ? fixA : ch.algo;
+  int P = fixP >= 0 ? fixP : ch.proto;
   if (n == 1) A = kRing;  // a single rank is a local copy (ncclLaunchOneRank)
   int C = comm->forceChannels ? comm->forceChannels
         : comm->envChannels   ? comm->envChannels

@@ -1,0 +1,143 @@
+"""Measure the auto-tuning table on this GPU, through the C ABI.
+
+NCCL fills its tuning tables from model constants and takes the smallest
+predicted time T = latency + bytes / bandwidth per (algorithm, protocol)
+("NCCL architecture: topology, channels, algorithms and protocols", §8.2).
+Here every (algo, proto, channels) candidate is timed at every power-of-two
+message size, and the table records the measured microseconds per call;
+``vrcclCommLoadTuning`` (or ``VRCCL_TUNE_FILE``) makes "auto" pick the
+measured minimum at the nearest size.
+
+Usage (on the GPU):
+    python -m ring_allreduce_reduction_gb300.tune --nranks 8 --dtype bfloat16 \\
+        --min-bytes 8 --max-bytes 4194304 --out table.txt
+
+Table format (one entry per line, '#' comments):
+    nranks algo proto channels log2bytes sliceBytes microseconds
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+import time
+
+import torch
+
+ELEM = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+TORCH = {"int32": torch.int32, "float32": torch.float32, "bfloat16": torch.bfloat16, "float16": torch.float16}
+
+
+def time_call(v, comm, sp, rp, count, dtype, op, algo, proto, iters, warmup, stream) -> float:
+    """Mean microseconds per call over `iters` back-to-back calls on one stream."""
+    for _ in range(warmup):
+        v.vrcclAllReduce(sp, rp, count, dtype, op, algo, proto, comm, stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        v.vrcclAllReduce(sp, rp, count, dtype, op, algo, proto, comm, stream)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / iters
+
+
+def sweep(nranks: int, dtype: str, sizes: list[int], protos: list[str], algos: list[str], channels: list[int],
+          op: str = "sum", max_channels: int = 32, iters: int = 30, warmup: int = 3, log=print) -> list[dict]:
+    """Time every candidate at every size; returns one record per point."""
+    from ring_allreduce_reduction_gb300 import vrccl as v
+    E = ELEM[dtype]
+    maxcount = max(sizes) // E
+    pad = (maxcount + 15) // 16 * 16
+    send = torch.zeros((nranks, pad), dtype=TORCH[dtype], device="cuda")
+    send.uniform_(-1, 1) if dtype != "int32" else send.random_(-1000, 1000)
+    recv = torch.empty_like(send)
+    sp = [send[r] for r in range(nranks)]
+    rp = [recv[r] for r in range(nranks)]
+    comm = v.vrcclCommInit(nranks, max_channels)
+    stream = torch.cuda.current_stream()
+    out = []
+    try:
+        for nbytes in sizes:
+            count = max(1, nbytes // E)
+            for algo in algos:
+                if algo == "tree" and nranks == 1:
+                    continue
+                for proto in protos:
+                    for nch in channels:
+                        if nch > max_channels:
+                            continue
+                        v.vrcclCommSetSchedule(comm, nch, 0)
+                        try:
+                            it = iters if nbytes <= (1 << 24) else max(3, iters // 10)
+                            us = time_call(v, comm, sp, rp, count, dtype, op, algo, proto, it, warmup, stream)
+                        except v.VrcclError as e:  # a shape this GPU cannot hold at once
+                            log(f"# skip n={nranks} {algo}/{proto} C={nch} {nbytes} B: {e}")
+                            continue
+                        sched = v.vrcclCommGetLastSchedule(comm)
+                        shape = v.vrcclCommGetLaunchShape(comm)
+                        rec = {"nranks": nranks, "dtype": dtype, "bytes": count * E, "algo": algo, "proto": proto,
+                               "channels": sched["nchannels"], "chunk_elems": sched["chunk_elems"],
+                               "slice_bytes": shape["slice_elems"] * E, "us": us,
+                               "busbw_gbs": count * E / (us * 1e-6) * (2 * (nranks - 1) / nranks if nranks > 1 else 1)
+                               / 1e9}
+                        out.append(rec)
+                        log(f"n={nranks} {dtype} {count * E:>11d} B {algo:4s} {proto:6s} C={sched['nchannels']:2d} "
+                            f"{us:10.2f} us  busbw {rec['busbw_gbs']:8.2f} GB/s")
+        err = v.vrcclCommGetAsyncError(comm)
+        if err:
+            raise RuntimeError(f"device error during the sweep: {v.RESULTS[err]}")
+    finally:
+        v.vrcclCommDestroy(comm)
+    return out
+
+
+def write_table(records: list[dict], path: str, header: str = "") -> None:
+    alg = {"ring": 0, "tree": 1}
+    pro = {"simple": 0, "ll": 1, "ll128": 2}
+    with open(path, "w") as f:
+        f.write("# vrccl tuning table: nranks algo proto channels log2bytes sliceBytes microseconds\n")
+        if header:
+            for ln in header.splitlines():
+                f.write(f"# {ln}\n")
+        for r in records:
+            log2 = max(0, int(r["bytes"]).bit_length() - 1)
+            f.write(f"{r['nranks']} {alg[r['algo']]} {pro[r['proto']]} {r['channels']} {log2} {r['slice_bytes']} "
+                    f"{r['us']:.3f}\n")
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--nranks", type=int, default=8)
+    ap.add_argument("--dtype", default="bfloat16", choices=list(ELEM))
+    ap.add_argument("--op", default="sum")
+    ap.add_argument("--min-bytes", type=int, default=8)
+    ap.add_argument("--max-bytes", type=int, default=4 << 20)
+    ap.add_argument("--protos", default="simple,ll,ll128")
+    ap.add_argument("--algos", default="ring,tree")
+    ap.add_argument("--channels", default="1,2,4,8,16,32")
+    ap.add_argument("--max-channels", type=int, default=32)
+    ap.add_argument("--iters", type=int, default=30)
+    ap.add_argument("--out", default="")
+    ap.add_argument("--json", default="")
+    args = ap.parse_args()
+    sizes, b = [], args.min_bytes
+    while b <= args.max_bytes:
+        sizes.append(b)
+        b *= 2
+    t0 = time.time()
+    recs = sweep(args.nranks, args.dtype, sizes, args.protos.split(","), args.algos.split(","),
+                 [int(c) for c in args.channels.split(",")], args.op, args.max_channels, args.iters)
+    if args.out:
+        write_table(recs, args.out, header=f"measured on {torch.cuda.get_device_name()} in {time.time() - t0:.0f} s, "
+                                           f"dtype {args.dtype}, op {args.op}")
+    if args.json:
+        import json
+        with open(args.json, "w") as f:
+            json.dump(recs, f)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    sys.exit(main())

@@ -65,3 +65,25 @@ def test_binding_names_match_the_c_names():
     from ring_allreduce_reduction_gb300 import vrccl
     for name in declared():
         assert hasattr(vrccl, name), f"binding lacks {name}"
+
+
+def test_tuning_table_writer_format(tmp_path):
+    """tune.write_table emits the line format the library parses:
+    nranks algo proto channels log2bytes sliceBytes microseconds."""
+    from ring_allreduce_reduction_gb300.tune import write_table
+    recs = [{"nranks": 8, "algo": "tree", "proto": "ll128", "channels": 3, "bytes": 1 << 20, "slice_bytes": 30720,
+             "us": 12.5}]
+    p = tmp_path / "t.txt"
+    write_table(recs, str(p), header="x")
+    rows = [ln.split() for ln in p.read_text().splitlines() if not ln.startswith("#")]
+    assert rows == [["8", "1", "2", "3", "20", "30720", "12.500"]]
+
+
+def test_shipped_tuning_table_parses():
+    path = os.path.join(ROOT, "ring_allreduce_reduction_gb300", "tuning", "gb300_n8.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert len(rows) > 100
+    for r in rows:
+        n, algo, proto, ch, lg, sl = map(int, r[:6])
+        assert n == 8 and algo in (0, 1) and proto in (0, 1, 2) and 1 <= ch <= 64 and 0 <= lg < 40 and sl > 0
+        assert float(r[6]) > 0

@@ -1,0 +1,154 @@
+"""Parity at the full sizes of the workloads, on sampled outputs.
+
+The oracle's association predictor (and, for the tree, the tree fold over
+the sampled columns) evaluates a few hundred thousand sampled elements of
+each result; every rank's recv buffer must equal rank 0's everywhere
+(compared on the device), and sampled results must match the oracle bit
+for bit and stay within the closed-form tolerance.
+"""
+import numpy as np
+import pytest
+
+from oracle import closed_form, ring as oring, schedule, tree as otree
+from ring_allreduce_reduction_gb300.workloads import ELEM_SIZE, STORAGE, bucket_sizes, make_inputs
+
+pytestmark = pytest.mark.gpu
+SAMPLES = 200_000
+
+
+@pytest.fixture(scope="module")
+def v():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ring_allreduce_reduction_gb300 import build
+    build.build()
+    from ring_allreduce_reduction_gb300 import vrccl
+    return vrccl
+
+
+def _device(x, dtype):
+    import torch
+    t = torch.from_numpy(x.view(np.int16) if dtype == "bfloat16" else x)
+    return t.to("cuda:0")
+
+
+def _sampled_check(v, comm, x, recv, dtype, op, seed=0):
+    import torch
+    n, count = x.shape
+    sched = v.vrcclCommGetLastSchedule(comm)
+    assert v.vrcclCommGetAsyncError(comm) == 0
+    for r in range(1, n):
+        assert torch.equal(recv[r], recv[0]), f"rank {r} differs from rank 0"
+    idx = np.sort(np.random.default_rng(seed).choice(count, min(SAMPLES, count), replace=False))
+    idx = np.unique(np.concatenate([idx, [0, count - 1]]))
+    got = recv[0].cpu().numpy()[idx].view(STORAGE[dtype])
+    if sched["algo"] == "ring":
+        ref = oring.ring_predict(x, op, dtype, sched["nchannels"], sched["chunk_elems"], idx)
+    else:
+        ref = _tree_sampled(x, op, dtype, sched["nchannels"], idx)
+    mism = np.nonzero(got.view(np.uint8).reshape(len(idx), -1) != ref.view(np.uint8).reshape(len(idx), -1))[0]
+    assert mism.size == 0, (sched, "first mismatching sampled indices", idx[np.unique(mism)][:5])
+    ok, worst = closed_form.check(got, x[:, idx], op, dtype)
+    assert ok, worst
+    return sched
+
+
+def _tree_sampled(x, op, dtype, nch, idx):
+    """The tree fold over sampled columns, grouped by the tree of their channel."""
+    from oracle import numerics as nm
+    n, count = x.shape
+    ranges = schedule.channel_ranges(count, nch, ELEM_SIZE[dtype])
+    his = np.array([hi for _, hi in ranges])
+    ch = np.searchsorted(his, idx, side="right")
+    which = np.array([schedule.channel_tree(int(c), nch) for c in ch])
+    out = np.empty(len(idx), dtype=STORAGE[dtype])
+    for t in (0, 1):
+        sel = np.nonzero(which == t)[0]
+        if not len(sel):
+            continue
+        sub = x[:, idx[sel]]
+        local = [nm.prescale(sub[r], op, dtype, n) for r in range(n)]
+        res = [np.empty(len(sel), dtype=STORAGE[dtype]) for _ in range(n)]
+        otree.tree_machine(local, lambda a, b: nm.combine(op, a, b, dtype), lambda y: nm.postop(y, op, dtype, n),
+                           otree.tree_links(n, t), slice(0, len(sel)), res)
+        out[sel] = res[0]
+    return out
+
+
+def test_bench_workload_fp32_256MiB(v):
+    """Exactly what bench.py times: n=8, 256 MiB/rank fp32 sum, ring, Simple,
+    32-channel communicator, channel count chosen by the library."""
+    import torch
+    n, count = 8, (256 << 20) // 4
+    x = make_inputs(n, count, "float32", "uniform", seed=1000)
+    send = _device(x, "float32")
+    recv = torch.empty_like(send)
+    comm = v.vrcclCommInit(n, 32)
+    try:
+        v.vrcclAllReduce([send[r] for r in range(n)], [recv[r] for r in range(n)], count, "float32", "sum",
+                         "ring", "simple", comm)
+        torch.cuda.synchronize()
+        sched = _sampled_check(v, comm, x, recv, "float32", "sum")
+        assert sched["proto"] == "simple" and sched["nchannels"] >= 16
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+def test_int32_256MiB_exact(v):
+    import torch
+    n, count = 8, (256 << 20) // 4
+    x = make_inputs(n, count, "int32", "int_uniform", seed=5, lo=-2**20, hi=2**20)
+    send = _device(x, "int32")
+    recv = torch.empty_like(send)
+    comm = v.vrcclCommInit(n, 32)
+    try:
+        v.vrcclAllReduce([send[r] for r in range(n)], [recv[r] for r in range(n)], count, "int32", "sum",
+                         "ring", "simple", comm)
+        torch.cuda.synchronize()
+        _sampled_check(v, comm, x, recv, "int32", "sum", seed=1)
+        # int32 sums are order-free: the whole buffer equals the closed form
+        ref = torch.from_numpy(x.astype(np.int64).sum(axis=0).astype(np.int32)).to("cuda:0")
+        assert torch.equal(recv[0], ref)
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("n", [16, 32, 72])
+def test_many_ranks_ring_and_tree_64MiB(v, n):
+    import torch
+    count = (64 << 20) // 4
+    x = make_inputs(n, count, "float32", "uniform", seed=n)
+    send = _device(x, "float32")
+    recv = torch.empty_like(send)
+    comm = v.vrcclCommInit(n, 32)
+    try:
+        for algo in ("ring", "tree"):
+            recv.fill_(0)
+            v.vrcclAllReduce([send[r] for r in range(n)], [recv[r] for r in range(n)], count, "float32", "sum",
+                             algo, "auto", comm)
+            torch.cuda.synchronize()
+            sched = _sampled_check(v, comm, x, recv, "float32", "sum", seed=2)
+            assert sched["algo"] == algo
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+def test_gradient_bucket_bf16_avg_1GiB(v):
+    """n=8, a 1 GiB/rank bf16 bucket of 224 log-uniform tensors (as one flat
+    buffer), values normal(0, 1e-3), op avg, algo and protocol auto."""
+    import torch
+    n, total = 8, 1 << 30
+    sizes = bucket_sizes(total, 224, 4 << 10, 64 << 20, seed=0, align=16)
+    assert len(sizes) == 224 and sum(sizes) == total
+    count = total // 2
+    x = make_inputs(n, count, "bfloat16", "normal", seed=7, std=1e-3)
+    send = _device(x, "bfloat16")
+    recv = torch.empty_like(send)
+    comm = v.vrcclCommInit(n, 32)
+    try:
+        v.vrcclAllReduce([send[r] for r in range(n)], [recv[r] for r in range(n)], count, "bfloat16", "avg",
+                         "auto", "auto", comm)
+        torch.cuda.synchronize()
+        _sampled_check(v, comm, x, recv, "bfloat16", "avg", seed=3)
+    finally:
+        v.vrcclCommDestroy(comm)

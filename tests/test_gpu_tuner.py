@@ -1,0 +1,69 @@
+"""The measured tuner: "auto" takes the table's fastest entry at the nearest
+measured size, among the entries the caller left free. Through the C ABI."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import ring as oring, tree as otree
+from ring_allreduce_reduction_gb300.workloads import make_inputs
+from tests.gpu_harness import run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def v():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ring_allreduce_reduction_gb300 import build
+    build.build()
+    from ring_allreduce_reduction_gb300 import vrccl
+    return vrccl
+
+
+def _check(x, y, sched):
+    if sched["algo"] == "tree":
+        ref = otree.tree_allreduce(x, "sum", "float32", sched["nchannels"])
+    else:
+        ref = oring.ring_allreduce(x, "sum", "float32", sched["nchannels"], sched["chunk_elems"])
+    assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+
+
+def test_auto_follows_the_measured_table(v, tmp_path):
+    n = 5
+    table = tmp_path / "table.txt"
+    # nranks algo proto channels log2bytes sliceBytes us ; 2^18 B = 65536 floats
+    table.write_text("# synthetic\n"
+                     "5 0 0 2 18 16384 10.0\n"   # ring simple C=2
+                     "5 1 2 3 18 30720 5.0\n"    # tree ll128 C=3  <- fastest overall
+                     "5 0 1 1 18 8192 7.0\n"     # ring ll C=1     <- fastest ring
+                     "5 0 0 4 10 16384 1.0\n"    # another size: must not be picked
+                     "7 0 0 1 18 16384 0.5\n")   # another rank count: ignored
+    comm = v.vrcclCommInit(n, 4)
+    try:
+        assert v.vrcclCommLoadTuning(comm, str(table)) == 4
+        x = make_inputs(n, 70000, "float32", "normal", seed=3)  # 280000 B: nearest measured size 2^18
+        for algo, proto, want in (("auto", "auto", ("tree", "ll128", 3)),
+                                  ("auto", "simple", ("ring", "simple", 2)),
+                                  ("ring", "auto", ("ring", "ll", 1))):
+            y, sched, _ = run(v, comm, x, "float32", "sum", algo, proto)
+            assert (sched["algo"], sched["proto"], sched["nchannels"]) == want, (algo, proto, sched)
+            _check(x, y, sched)
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+def test_shipped_table_is_found_for_8_ranks(v):
+    from ring_allreduce_reduction_gb300 import vrccl
+    path = os.path.join(os.path.dirname(vrccl.LIB_PATH), "tuning", "gb300_n8.txt")
+    assert os.path.exists(path)
+    comm = v.vrcclCommInit(8, 32)
+    try:
+        # tiny message: the measured table says LL (ring or tree), not Simple
+        x = make_inputs(8, 64, "float32", "normal", seed=4)
+        y, sched, _ = run(v, comm, x, "float32", "sum", "auto", "auto")
+        assert sched["proto"] == "ll"
+        _check(x, y, sched)
+    finally:
+        v.vrcclCommDestroy(comm)
