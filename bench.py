@@ -86,11 +86,13 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ring_simple_n8_fp32_256MiB.md"
 
 
 def kernel_sources_sha256() -> str:
-    """Hash of the library sources: ties an ncu summary to the kernel it measured."""
+    """Hash of the device-side sources (kernel translation units, device
+    headers, the shared layout header): ties an ncu summary to the kernel it
+    measured. Host-only files (the launcher, the tuner) do not enter."""
     import hashlib
     h = hashlib.sha256()
     for f in sorted(os.listdir(KERNEL_SOURCES)):
-        if f.endswith((".cu", ".cuh", ".h", ".cc")):
+        if f.endswith(".cuh") or (f.startswith("kernels_") and f.endswith(".cu")) or f == "vrccl_internal.h":
             with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
