@@ -25,6 +25,8 @@ Modules:
                   plus an independent association predictor.
 * ``tree``        the double-binary-tree AllReduce (reduce up, broadcast
                   down).
+* ``phases``      the reduce-scatter and all-gather phases of the ring run
+                  alone (ReduceScatter, AllGather), with a predictor.
 * ``closed_form`` the order-free definition (float64 / exact integers) and
                   the error bounds it is compared under.
 
@@ -32,6 +34,6 @@ Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, brute force on tiny inputs, invariants and the
 worked examples the pages print (``tests/golden/``).
 """
-from . import numerics, schedule, ring, tree, closed_form  # noqa: F401
+from . import numerics, schedule, ring, tree, phases, closed_form  # noqa: F401
 from .ring import ring_allreduce, ring_predict  # noqa: F401
 from .tree import tree_allreduce  # noqa: F401
