@@ -15,6 +15,9 @@ Reported (one JSON line on rank 0):
   cpu_baseline  the CPU oracle replaying the same schedule on a bounded
             sample of the workload, on the host cores
 `--impl reference` times that oracle alone (the reference arm).
+`--coll reduce_scatter|all_gather` times one of the ring's two phases run
+alone on the same n, dtype and 256 MiB per-rank buffer (ReduceScatter: the
+send buffer; AllGather: the recv buffer) instead of the AllReduce.
 
 Launch: python bench.py [--gpus N] [--steps K] [--warmup W]; for N > 1 under
 torchrun (one process per GPU, RANK/LOCAL_RANK/WORLD_SIZE from the env).
@@ -46,6 +49,11 @@ WORKLOAD = {
     "max_channels": 32,
 }
 METRIC = "allreduce busbw (n=8 virtual ranks, 256 MiB/rank fp32 sum, ring Simple)"
+COLL_METRIC = {
+    "allreduce": METRIC,
+    "reduce_scatter": "reduce_scatter busbw (n=8 virtual ranks, 256 MiB/rank send fp32 sum, ring Simple)",
+    "all_gather": "all_gather busbw (n=8 virtual ranks, 256 MiB/rank recv fp32, ring Simple)",
+}
 ELEM = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
 
 
@@ -73,12 +81,15 @@ def rank_seed(rank: int) -> int:
     return 1000 + rank
 
 
-def busbw_gbs(bytes_per_rank: int, n: int, seconds: float) -> float:
+def busbw_gbs(bytes_per_rank: int, n: int, seconds: float, coll: str = "allreduce") -> float:
     """busbw = algbw * 2(n-1)/n with algbw = S / t ("NCCL architecture ...",
-    introduction: the ring moves 2(n-1)/n * S per rank)."""
+    introduction: the ring moves 2(n-1)/n * S per rank). Each phase alone
+    moves half of that, (n-1)/n * S per rank, with S the per-rank buffer
+    that holds all n blocks."""
     if n == 1:
         return bytes_per_rank / seconds / 1e9
-    return bytes_per_rank / seconds * 2 * (n - 1) / n / 1e9
+    f = 2 if coll == "allreduce" else 1
+    return bytes_per_rank / seconds * f * (n - 1) / n / 1e9
 
 
 KERNEL_SOURCES = os.path.join(ROOT, "ring_allreduce_reduction_gb300", "csrc")
@@ -184,23 +195,27 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(x: np.ndarray, dtype: str, op: str, nch: int, chunk_elems: int, min_seconds: float = 10.0) -> dict:
+def cpu_baseline(x: np.ndarray, dtype: str, op: str, nch: int, chunk_elems: int, min_seconds: float = 10.0,
+                 coll: str = "allreduce") -> dict:
     """The oracle as it stands on the bench's own inputs, replaying the
     schedule the GPU ran (same channels and chunk), repeated until about
     `min_seconds` of CPU time (at most 5 runs)."""
-    from oracle import ring as oring
+    from oracle import phases, ring as oring
     n, count = x.shape
+    run = {"allreduce": lambda: oring.ring_allreduce(x, op, dtype, nch, chunk_elems),
+           "reduce_scatter": lambda: phases.ring_reduce_scatter(x, op, dtype),
+           "all_gather": lambda: phases.ring_all_gather(x)}[coll]
     times = []
     while True:
         t0 = time.perf_counter()
-        oring.ring_allreduce(x, op, dtype, nch, chunk_elems)
+        run()
         times.append(time.perf_counter() - t0)
         if sum(times) >= min_seconds or len(times) >= 5:
             break
     dt = statistics.mean(times)
-    S = count * ELEM[dtype]
-    return {"value": round(busbw_gbs(S, n, dt), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"the whole workload: n={n} x {count} {dtype} per rank ({S >> 20} MiB/rank), {nch} channels, "
+    S = count * ELEM[dtype] * (n if coll == "all_gather" else 1)
+    return {"value": round(busbw_gbs(S, n, dt, coll), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole workload: n={n} x {count} {dtype} per rank send buffer, {coll}, {nch} channels, "
                       f"chunk {chunk_elems} elements; numpy step machine, one thread; {len(times)} run(s), "
                       f"mean {dt:.2f} s"}
 
@@ -263,6 +278,8 @@ def main() -> int:
     ap.add_argument("--ref-budget", type=float, default=150.0, help="seconds the reference arm aims to take")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    ap.add_argument("--coll", default="allreduce", choices=["allreduce", "reduce_scatter", "all_gather"],
+                    help="allreduce (the workload), or one of its two ring phases run alone")
     ap.add_argument("--bytes-per-rank", type=int, default=0,
                     help="profiling only: a smaller per-rank size than the workload's (reported in config)")
     args = ap.parse_args()
@@ -286,21 +303,30 @@ def main() -> int:
     from ring_allreduce_reduction_gb300.workloads import make_inputs
 
     W = dict(WORKLOAD)
+    coll = args.coll
+    if coll != "allreduce":
+        W["name"] = W["name"].replace("_sum_", "_sum_" + coll + "_")
     if args.bytes_per_rank:
         W["bytes_per_rank"] = args.bytes_per_rank
         W["name"] += f" (profiling size {args.bytes_per_rank} B/rank)"
     n, dtype = W["nranks"], W["dtype"]
     S = W["bytes_per_rank"]
-    count = S // ELEM[dtype]
-    x = make_inputs(n, count, dtype, "uniform", seed=rank_seed(rank))
+    count = S // ELEM[dtype]           # elements of the per-rank buffer that holds all n blocks
+    block = count // n                 # phases: elements per block
+    x = make_inputs(n, block if coll == "all_gather" else count, dtype, "uniform", seed=rank_seed(rank))
     send = torch.from_numpy(x).cuda()
-    recv = torch.empty_like(send)
+    recv = torch.empty((n, block) if coll == "reduce_scatter" else (n, count), dtype=send.dtype, device=send.device)
     sp, rp = [send[r] for r in range(n)], [recv[r] for r in range(n)]
     comm = v.vrcclCommInit(n, W["max_channels"])
     stream = torch.cuda.current_stream()
 
     def step():
-        v.vrcclAllReduce(sp, rp, count, dtype, W["op"], W["algo"], W["proto"], comm, stream)
+        if coll == "allreduce":
+            v.vrcclAllReduce(sp, rp, count, dtype, W["op"], W["algo"], W["proto"], comm, stream)
+        elif coll == "reduce_scatter":
+            v.vrcclReduceScatter(sp, rp, block, dtype, W["op"], W["proto"], comm, stream)
+        else:
+            v.vrcclAllGather(sp, rp, block, dtype, W["proto"], comm, stream)
 
     for _ in range(args.warmup):
         step()
@@ -335,14 +361,16 @@ def main() -> int:
         raise RuntimeError(f"device error in the timed region: {v.RESULTS[err]}")
     total_ms = max_over_ranks(total_ms, "cuda")
     ms_step = total_ms / args.steps
-    value = busbw_gbs(S, n, ms_step / 1e3) * world
+    value = busbw_gbs(S, n, ms_step / 1e3, coll) * world
 
-    # roofline of the one kernel: essential bytes / mean launch time
-    algo_bytes = 2 * n * S
+    # roofline of the one kernel: essential bytes / mean launch time. The
+    # AllReduce reads n inputs and writes n outputs (2 n S); a phase reads
+    # and writes n S + S (n full buffers one way, n blocks the other).
+    algo_bytes = 2 * n * S if coll == "allreduce" else (n + 1) * S
     mean_kern_s = statistics.mean(kern_ms) / 1e3
     peak, peak_kind = measured_peak()
     achieved = algo_bytes / mean_kern_s / 1e9
-    traffic = profiled_traffic(S)
+    traffic = profiled_traffic(S) if coll == "allreduce" else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
@@ -352,7 +380,7 @@ def main() -> int:
     e2e = None
     if not args.no_e2e:
         host_in = torch.from_numpy(x).pin_memory()
-        host_out = torch.empty_like(host_in).pin_memory()
+        host_out = torch.empty(recv.shape, dtype=recv.dtype).pin_memory()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -365,20 +393,22 @@ def main() -> int:
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
         e2e_ms = max_over_ranks(e2e_ms, "cuda")
-        e2e = {"value": round(busbw_gbs(S, n, e2e_ms / 1e3) * world, 3), "unit": "GB/s",
-               "h2d_bytes_per_step": n * S, "d2h_bytes_per_step": n * S, "ms_per_step": round(e2e_ms, 3)}
+        e2e = {"value": round(busbw_gbs(S, n, e2e_ms / 1e3, coll) * world, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": round(e2e_ms, 3)}
 
     v.vrcclCommDestroy(comm)
     if rank != 0:
         return 0
     cpu = None
     if not args.no_cpu:
-        cpu = cpu_baseline(x, dtype, W["op"], sched["nchannels"], sched["chunk_elems"])
+        cpu = cpu_baseline(x, dtype, W["op"], sched["nchannels"], sched["chunk_elems"], coll=coll)
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "metric": COLL_METRIC[coll], "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": W["name"], "nranks": n, "bytes_per_rank": S, "count": count, "op": W["op"],
+        "config": {"workload": W["name"], "coll": coll, "nranks": n, "bytes_per_rank": S, "count": count,
+                   "op": W["op"],
                    "algo": sched["algo"], "proto": sched["proto"], "channels": sched["nchannels"],
                    "chunk_elems": sched["chunk_elems"], "blocks": shape["blocks"], "threads": shape["threads"],
                    "slice_elems": shape["slice_elems"],

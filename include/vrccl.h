@@ -178,6 +178,54 @@ vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const* recvbufs,
                              vrcclProto_t proto, vrcclComm_t comm, vrcclStream_t stream);
 
 /*
+ * vrcclReduceScatter -- the reduce-scatter phase of the ring AllReduce run
+ * alone [Deep Dive §2.3: the AllReduce is a reduce-scatter phase and an
+ * all-gather phase of n-1 steps each]. Block r of every rank's send buffer
+ * is reduced into rank r's recv buffer, one launch on `stream`. The pages
+ * give the phase, not a buffer contract; NCCL's ncclReduceScatter contract
+ * is followed.
+ *   sendbufs  host array of n device pointers; sendbufs[r] holds n blocks
+ *             of `recvcount` elements (block q = elements [q*recvcount,
+ *             (q+1)*recvcount)). Read during the call only.
+ *   recvbufs  host array of n device pointers; recvbufs[r] receives
+ *             `recvcount` elements: element e = op over ranks of their
+ *             block r, element e, associated in ring order
+ *             op(...op(x[r+1], x[r+2])..., x[r]). In place:
+ *             recvbufs[r] == sendbufs[r] + r*recvcount elements.
+ *   recvcount elements per block; recvcount * element size must be a
+ *             multiple of 16 bytes when n > 1, so that every block starts
+ *             on a 16-byte boundary. 0 -> success, nothing launched.
+ *   dtype, op as for vrcclAllReduce (avg: the same pre-scale / post-op).
+ *   proto     simple, ll, ll128, or auto. The schedule is the ring.
+ * Channels split each block; a loop takes one chunk of every block. Errors
+ * as for vrcclAllReduce, plus vrcclInvalidArgument for a block that is not
+ * a multiple of 16 bytes.
+ */
+vrcclResult_t vrcclReduceScatter(const void* const* sendbufs, void* const* recvbufs, size_t recvcount,
+                                 vrcclDataType_t dtype, vrcclRedOp_t op, vrcclProto_t proto,
+                                 vrcclComm_t comm, vrcclStream_t stream);
+
+/*
+ * vrcclAllGather -- the all-gather phase of the ring AllReduce run alone
+ * [Deep Dive §2.3]: rank q's send buffer lands as block q of every rank's
+ * recv buffer, bit for bit, one launch on `stream`. NCCL's ncclAllGather
+ * contract is followed.
+ *   sendbufs  host array of n device pointers; sendbufs[r] holds
+ *             `sendcount` elements. Read during the call only.
+ *   recvbufs  host array of n device pointers; recvbufs[r] receives n
+ *             blocks of `sendcount` elements. In place:
+ *             sendbufs[r] == recvbufs[r] + r*sendcount elements.
+ *   sendcount elements per block, with the same 16-byte rule as
+ *             vrcclReduceScatter. 0 -> success, nothing launched.
+ *   dtype     any type; the data moves as 4-byte words (no arithmetic).
+ *   proto     simple, ll, ll128, or auto. The schedule is the ring.
+ * Errors as for vrcclReduceScatter.
+ */
+vrcclResult_t vrcclAllGather(const void* const* sendbufs, void* const* recvbufs, size_t sendcount,
+                             vrcclDataType_t dtype, vrcclProto_t proto, vrcclComm_t comm,
+                             vrcclStream_t stream);
+
+/*
  * vrcclCommSetSchedule -- pin the channel count and chunk size used by
  * later calls (0 = choose automatically, the default).
  *   nchannels  0, or 1..the communicator's nchannels.

@@ -43,10 +43,12 @@ __global__ void __launch_bounds__(1024) ringKernel(const __grid_constant__ KArgs
   const int r = blockIdx.x % n, ch = blockIdx.x / n;
   const DevComm& c = a.comm;
   if (aborted(c)) return;
+  // AllReduce: channels split the buffer; the phases: channels split a
+  // block, and every loop visits the same range of each block.
   unsigned long long lo, hi;
   channelRange<S>(a.count, a.nchannels, ch, lo, hi);
-  const char* in = reinterpret_cast<const char*>(a.send[r]) + lo * E;
-  char* out = reinterpret_cast<char*>(a.recv[r]) + lo * E;
+  const char* in = reinterpret_cast<const char*>(a.send[r]);
+  char* out = reinterpret_cast<char*>(a.recv[r]);
 
   Agent ag;
   ag.init(c, PROTO, r, ch);
@@ -55,13 +57,14 @@ __global__ void __launch_bounds__(1024) ringKernel(const __grid_constant__ KArgs
     ag.addSend(c, ringEdge(ch, r, n));
   }
   RingIter it;
-  it.init(n, r, (long long)(hi - lo), a.chunkElems, 16 / E, a.sliceElems);
+  it.init(n, r, a.coll, (long long)lo, (long long)(hi - lo), (long long)a.count, a.chunkElems, 16 / E,
+          a.sliceElems);
   if constexpr (PROTO == kSimple) {
     simplePipeline<DT, OP, false>(a, ag, it, in, out);
   } else {
     SliceDesc d;
     while (it.next(d))
-      if (!runSlice<PROTO, DT, OP, false>(a, ag, in + d.pos * E, out + d.pos * E, d.nelem, d.flags)) return;
+      if (!runSlice<PROTO, DT, OP, false>(a, ag, in + d.inPos * E, out + d.outPos * E, d.nelem, d.flags)) return;
     ag.finish(c);
   }
 }
@@ -172,16 +175,16 @@ __global__ void __launch_bounds__(1024) treeKernel(const __grid_constant__ KArgs
 
   unsigned long long lo, hi;
   channelRange<S>(a.count, a.nchannels, ch, lo, hi);
-  const char* in = reinterpret_cast<const char*>(a.send[rank]) + lo * E;
-  char* out = reinterpret_cast<char*>(a.recv[rank]) + lo * E;
+  const char* in = reinterpret_cast<const char*>(a.send[rank]);
+  char* out = reinterpret_cast<char*>(a.recv[rank]);
   TreeIter it;
-  it.init((long long)(hi - lo), a.sliceElems, flags);
+  it.init((long long)lo, (long long)(hi - lo), a.sliceElems, flags);
   if constexpr (PROTO == kSimple) {
     simplePipeline<DT, OP, true>(a, ag, it, in, out);
   } else {
     SliceDesc d;
     while (it.next(d))
-      if (!runSlice<PROTO, DT, OP, true>(a, ag, in + d.pos * E, out + d.pos * E, d.nelem, d.flags)) return;
+      if (!runSlice<PROTO, DT, OP, true>(a, ag, in + d.inPos * E, out + d.outPos * E, d.nelem, d.flags)) return;
     ag.finish(c);
   }
 }

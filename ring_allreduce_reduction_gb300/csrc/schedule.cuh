@@ -8,7 +8,8 @@
 namespace vrccl {
 
 struct SliceDesc {
-  long long pos;  // element offset within the channel
+  long long inPos;   // element offset of the slice in this agent's send buffer
+  long long outPos;  // element offset of the slice in this agent's recv buffer
   int nelem;
   int flags;
 };
@@ -26,53 +27,90 @@ struct SliceDesc {
 // A loop covers n*K elements; a shorter remainder uses chunks of
 // alignUp(ceil(rem/n), 16 bytes). A chunk is cut into slices of at most
 // `slice` elements, one FIFO step each. With n == 1 the sequence is a copy.
+//
+// The two phases run alone ("NCCL Source Code Deep Dive", §2.3 walks the
+// AllReduce as a reduce-scatter phase and an all-gather phase of n-1 steps
+// each) use the same chunk order on blocks instead of loop chunks. The
+// channel range [lo, lo + chCount) is then a range within a block of `blk`
+// elements, a loop takes K elements of every block, and chunk c of a loop
+// lives in block c:
+//   ReduceScatter  p = 0 send c = r-1; p = 1..n-2 recvReduceSend c = r-1-p;
+//                  p = n-1 recvReduceCopy (post-op) c = r -> recv buffer
+//   AllGather      p = 0 copySend c = r (own send buffer -> block r);
+//                  p = 1..n-2 recvCopySend c = r-p; p = n-1 recv c = r+1
 struct RingIter {
-  int n, r;
-  long long chCount, K, A, slice;
-  long long off, rem, k, s, cHi;
-  int p, flags;
+  int n, r, coll;
+  long long chCount, K, A, slice, lo, blk;
+  long long off, rem, k;                // loop offset and remainder; chunk size of the loop
+  long long inBase, outBase, len, s;    // current chunk: slices [s, len) from the two bases
+  int p, nprim, flags;
   bool started;
 
-  __device__ __forceinline__ void init(int n_, int r_, long long chCount_, long long K_, long long A_,
-                                       long long slice_) {
+  __device__ __forceinline__ void init(int n_, int r_, int coll_, long long lo_, long long chCount_, long long blk_,
+                                       long long K_, long long A_, long long slice_) {
     n = n_;
     r = r_;
+    coll = coll_;
+    lo = lo_;
     chCount = chCount_;
+    blk = blk_;
     K = K_;
     A = A_;
     slice = slice_;
+    nprim = coll == kAllReduce ? 2 * n - 1 : n;
     started = false;
-    s = cHi = 0;
+    s = len = 0;
+    inBase = outBase = 0;
     p = 0;
     off = 0;
     flags = 0;
   }
+  __device__ __forceinline__ static int mod(int x, int m) { return ((x % m) + m) % m; }
   __device__ __forceinline__ void setChunk() {
     int c;
-    if (p == 0) {
-      c = (r - 1 + n) % n;
-      flags = F_IN | F_SEND;
-    } else if (p <= n - 2) {
-      c = ((r - 1 - p) % n + n) % n;
-      flags = F_IN | F_RECV | F_SEND;
-    } else if (p == n - 1) {
-      c = r;
-      flags = F_IN | F_RECV | F_POST | F_OUT | F_SEND;
-    } else if (p <= 2 * n - 3) {
-      c = ((r - (p - n + 1)) % n + n) % n;
-      flags = F_RECV | F_OUT | F_SEND;
+    if (coll == kAllReduce) {
+      if (p == 0) {
+        c = mod(r - 1, n);
+        flags = F_IN | F_SEND;
+      } else if (p <= n - 2) {
+        c = mod(r - 1 - p, n);
+        flags = F_IN | F_RECV | F_SEND;
+      } else if (p == n - 1) {
+        c = r;
+        flags = F_IN | F_RECV | F_POST | F_OUT | F_SEND;
+      } else if (p <= 2 * n - 3) {
+        c = mod(r - (p - n + 1), n);
+        flags = F_RECV | F_OUT | F_SEND;
+      } else {
+        c = mod(r + 1, n);
+        flags = F_RECV | F_OUT;
+      }
+      const long long cLo = min(rem, (long long)c * k);
+      len = min(rem, (long long)(c + 1) * k) - cLo;
+      inBase = outBase = lo + off + cLo;
+    } else if (coll == kReduceScatter) {
+      c = p == n - 1 ? r : mod(r - 1 - p, n);
+      flags = p == 0 ? (F_IN | F_SEND) : p < n - 1 ? (F_IN | F_RECV | F_SEND) : (F_IN | F_RECV | F_POST | F_OUT);
+      len = k;
+      inBase = (long long)c * blk + lo + off;
+      outBase = lo + off;
     } else {
-      c = (r + 1) % n;
-      flags = F_RECV | F_OUT;
+      c = mod(r - p, n);
+      flags = p == 0 ? (F_IN | F_OUT | F_SEND) : p < n - 1 ? (F_RECV | F_OUT | F_SEND) : (F_RECV | F_OUT);
+      len = k;
+      inBase = lo + off;
+      outBase = (long long)c * blk + lo + off;
     }
-    const long long cLo = min(rem, (long long)c * k);
-    cHi = off + min(rem, (long long)(c + 1) * k);
-    s = off + cLo;
+    s = 0;
   }
   __device__ __forceinline__ void setLoop() {
     rem = chCount - off;
-    const long long loop = (long long)n * K;
-    k = rem >= loop ? K : ((rem + n - 1) / n + A - 1) / A * A;
+    if (coll == kAllReduce) {
+      const long long loop = (long long)n * K;
+      k = rem >= loop ? K : ((rem + n - 1) / n + A - 1) / A * A;
+    } else {
+      k = min(rem, K);
+    }
   }
   __device__ __forceinline__ bool next(SliceDesc& d) {
     if (n == 1) {  // single rank: the local copy
@@ -81,16 +119,17 @@ struct RingIter {
         s = 0;
       }
       if (s >= chCount) return false;
-      d.pos = s;
+      d.inPos = d.outPos = lo + s;
       d.nelem = (int)min(slice, chCount - s);
       d.flags = F_IN | F_OUT | F_POST;
       s += slice;
       return true;
     }
     while (true) {
-      if (s < cHi) {
-        d.pos = s;
-        d.nelem = (int)min(slice, cHi - s);
+      if (s < len) {
+        d.inPos = inBase + s;
+        d.outPos = outBase + s;
+        d.nelem = (int)min(slice, len - s);
         d.flags = flags;
         s += slice;
         return true;
@@ -101,8 +140,8 @@ struct RingIter {
         off = 0;
         p = 0;
         setLoop();
-      } else if (++p == 2 * n - 1) {
-        off += (long long)n * K;
+      } else if (++p == nprim) {
+        off += coll == kAllReduce ? (long long)n * K : K;
         if (off >= chCount) return false;
         p = 0;
         setLoop();
@@ -114,9 +153,10 @@ struct RingIter {
 
 // Tree: the channel's range in slices, every slice with the role's flags.
 struct TreeIter {
-  long long chCount, slice, s;
+  long long lo, chCount, slice, s;
   int flags;
-  __device__ __forceinline__ void init(long long chCount_, long long slice_, int flags_) {
+  __device__ __forceinline__ void init(long long lo_, long long chCount_, long long slice_, int flags_) {
+    lo = lo_;
     chCount = chCount_;
     slice = slice_;
     flags = flags_;
@@ -124,7 +164,7 @@ struct TreeIter {
   }
   __device__ __forceinline__ bool next(SliceDesc& d) {
     if (s >= chCount) return false;
-    d.pos = s;
+    d.inPos = d.outPos = lo + s;
     d.nelem = (int)min(slice, chCount - s);
     d.flags = flags;
     s += slice;

@@ -117,7 +117,7 @@ __device__ void simplePipeline(const KArgs& a, Agent& ag, It it, const char* in,
     bool pmore = a.prefetch > 0;
     for (int k = 0; k < a.prefetch && pmore; ++k) {
       pmore = ahead.next(pd);
-      if (pmore && (pd.flags & F_IN) && pd.nelem * E >= 16) bulkPrefetchL2(in + pd.pos * E, unsigned(pd.nelem * E / 16 * 16));
+      if (pmore && (pd.flags & F_IN) && pd.nelem * E >= 16) bulkPrefetchL2(in + pd.inPos * E, unsigned(pd.nelem * E / 16 * 16));
     }
     SliceDesc d;
     long long q = 0;
@@ -126,7 +126,7 @@ __device__ void simplePipeline(const KArgs& a, Agent& ag, It it, const char* in,
       const int st = (int)(q % NST);
       const int use = (int)(q / NST);
       if (pmore && (pmore = ahead.next(pd)) && (pd.flags & F_IN) && pd.nelem * E >= 16)
-        bulkPrefetchL2(in + pd.pos * E, unsigned(pd.nelem * E / 16 * 16));
+        bulkPrefetchL2(in + pd.inPos * E, unsigned(pd.nelem * E / 16 * 16));
       if (!pipeWait(c, ag, &sh, &sh.empty[st], (use & 1) ^ 1)) {
         ok = false;
         break;
@@ -135,7 +135,7 @@ __device__ void simplePipeline(const KArgs& a, Agent& ag, It it, const char* in,
       if (inBytes) {
         lastUse[st] = use;
         mbarExpectTx(&sh.fullIn[st], inBytes);
-        bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes, in + d.pos * E, inBytes, &sh.fullIn[st]);
+        bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes, in + d.inPos * E, inBytes, &sh.fullIn[st]);
       }
       mbarArrive(&sh.fullIn[st]);
       ++q;
@@ -261,7 +261,7 @@ __device__ void simplePipeline(const KArgs& a, Agent& ag, It it, const char* in,
     const bool rv = (d.flags & F_RECV) && ag.nrecv > 0;
     char* dst0 = (d.flags & F_SEND) && ag.nsend > 0 ? ag.slot(c, ag.se[0], ag.sstep[0]) : nullptr;
     char* dst1 = (d.flags & F_SEND) && ag.nsend > 1 ? ag.slot(c, ag.se[1], ag.sstep[1]) : nullptr;
-    char* o = out + d.pos * E;
+    char* o = out + d.outPos * E;
     const int nv = d.nelem / V;
     for (int i = ct; i < nv; i += CT) {
       const size_t b = size_t(i) * 16;
@@ -278,7 +278,7 @@ __device__ void simplePipeline(const KArgs& a, Agent& ag, It it, const char* in,
       if (d.flags & F_OUT) stStream16(o + b, av);
     }
     for (int j = nv * V + ct; j < d.nelem; j += CT) {  // ragged end of the user buffer
-      S x = (d.flags & F_IN) ? reinterpret_cast<const S*>(in + d.pos * E)[j] : S(0);
+      S x = (d.flags & F_IN) ? reinterpret_cast<const S*>(in + d.inPos * E)[j] : S(0);
       S r0 = rv ? reinterpret_cast<const S*>(sR0)[j] : S(0);
       S r1 = (rv && ag.nrecv > 1) ? reinterpret_cast<const S*>(sR1)[j] : S(0);
       S v = reduceElem<DT, OP, TREE>(x, r0, r1, d.flags, ag.nrecv, a.scale, a.nranks);

@@ -368,12 +368,25 @@ static bool pickSimpleShape(const vrcclComm* c, const void* fn, int agents, int 
 
 static int agentsPerChannel(int algo, int n) { return algo == kRing ? n : 2 * n - 1; }
 
-static bool overlapFree(const void* const* s, void* const* r, int n, size_t bytes) {
+// The 2n buffers of a call, as byte ranges, must not overlap, except that a
+// recv buffer may sit at its in-place position: the send buffer itself
+// (AllReduce), block r of rank r's send buffer (ReduceScatter), or the
+// range holding block r of rank r's recv buffer (AllGather).
+static bool overlapFree(int coll, const void* const* s, void* const* r, int n, size_t sendBytes,
+                        size_t recvBytes) {
   std::vector<std::pair<uintptr_t, uintptr_t>> iv;
   iv.reserve(2 * n);
   for (int i = 0; i < n; ++i) {
-    iv.push_back({(uintptr_t)s[i], (uintptr_t)s[i] + bytes});
-    if (r[i] != s[i]) iv.push_back({(uintptr_t)r[i], (uintptr_t)r[i] + bytes});
+    const uintptr_t sb = (uintptr_t)s[i], rb = (uintptr_t)r[i];
+    const bool inPlace = coll == kAllReduce      ? rb == sb
+                       : coll == kReduceScatter ? rb == sb + size_t(i) * recvBytes
+                                                : sb == rb + size_t(i) * sendBytes;
+    if (inPlace) {
+      iv.push_back(coll == kAllGather ? std::make_pair(rb, rb + recvBytes) : std::make_pair(sb, sb + sendBytes));
+    } else {
+      iv.push_back({sb, sb + sendBytes});
+      iv.push_back({rb, rb + recvBytes});
+    }
   }
   std::sort(iv.begin(), iv.end());
   for (size_t i = 1; i < iv.size(); ++i)
@@ -381,9 +394,14 @@ static bool overlapFree(const void* const* s, void* const* r, int n, size_t byte
   return true;
 }
 
-extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const* recvbufs, size_t count,
-                                        vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo,
-                                        vrcclProto_t proto, vrcclComm_t comm, vrcclStream_t stream) {
+static const char* kCollName[3] = {"AllReduce", "ReduceScatter", "AllGather"};
+
+// One collective call: validate, choose the schedule, launch once.
+//   coll   AllReduce: count = elements per rank. ReduceScatter / AllGather:
+//          count = elements per block (recvcount / sendcount).
+static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const* recvbufs, size_t count,
+                             vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo, vrcclProto_t proto,
+                             vrcclComm_t comm, vrcclStream_t stream) {
   // Argument checks first (ncclEnqueueCheck: CommCheck, then ArgsCheck,
   // Deep Dive (Japanese edition) ch.6).
   if (!validComm(comm)) return vrcclInvalidArgument;
@@ -397,8 +415,14 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
     if (((uintptr_t)sendbufs[r] | (uintptr_t)recvbufs[r]) & 15u) return vrcclInvalidArgument;
   }
   const size_t E = kElemSize[dtype];
-  if (count > (size_t(1) << 40) / E) return vrcclInvalidArgument;
-  if (!overlapFree(sendbufs, recvbufs, n, count * E)) return vrcclInvalidArgument;
+  const size_t blocks = coll == kAllReduce ? 1 : (size_t)n;
+  if (count > (size_t(1) << 40) / E / blocks) return vrcclInvalidArgument;
+  // Every block of the phases starts on a 16-byte boundary, like a buffer.
+  if (coll != kAllReduce && n > 1 && (count * E) % 16) return vrcclInvalidArgument;
+  const size_t blockBytes = count * E;
+  const size_t sendBytes = coll == kReduceScatter ? blockBytes * n : blockBytes;
+  const size_t recvBytes = coll == kAllGather ? blockBytes * n : blockBytes;
+  if (!overlapFree(coll, sendbufs, recvbufs, n, sendBytes, recvBytes)) return vrcclInvalidArgument;
   if (comm->failed || comm->aborted) return vrcclInvalidUsage;
   if (count == 0) return vrcclSuccess;  // taskAppend step 4: nothing to do
 
@@ -406,10 +430,25 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
   cudaGetDevice(&dev);
   if (dev != comm->device) return vrcclInvalidUsage;
 
+  // The all-gather phase only copies: it runs as 4-byte words, whatever
+  // the type (the blocks are whole 16-byte units).
+  int kdtype = dtype, kop = op;
+  size_t kcount = count, kE = E;
+  if (coll == kAllGather) {
+    kdtype = vrcclInt32;
+    kop = vrcclSum;
+    kcount = n > 1 ? blockBytes / 4 : count;
+    kE = n > 1 ? 4 : E;
+    if (n == 1) kdtype = dtype;  // a single rank is a plain copy in the user's type
+  }
+
   // ---- schedule: algo, proto, channels, chunk, slice, threads
-  const size_t bytes = count * E;
-  const bool userAlgo = algo != vrcclAlgoAuto, userProto = proto != vrcclProtoAuto;
-  const int fixA = userAlgo ? (int)algo : comm->envAlgo, fixP = userProto ? (int)proto : comm->envProto;
+  // bytes = one rank's send (AllReduce, ReduceScatter) or recv (AllGather)
+  // buffer; the phases take the ring's entries of the table at that size.
+  const size_t bytes = coll == kAllReduce ? blockBytes : blockBytes * n;
+  const bool userAlgo = coll == kAllReduce && algo != vrcclAlgoAuto, userProto = proto != vrcclProtoAuto;
+  const int fixA = coll != kAllReduce ? kRing : userAlgo ? (int)algo : comm->envAlgo;
+  const int fixP = userProto ? (int)proto : comm->envProto;
   Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, n == 1 ? kRing : fixA, fixP);
   int A = fixA >= 0 ? fixA : ch.algo;
   int P = fixP >= 0 ? fixP : ch.proto;
@@ -420,7 +459,7 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
                            : defaultChannels(P, bytes, n, comm->maxChannels));
   const bool userChannels = comm->forceChannels || comm->envChannels;
 
-  const void* fn = kernelFor(A, P, dtype, op);
+  const void* fn = kernelFor(A, P, kdtype, kop);
   if (!fn) return vrcclInternalError;
   const int per = agentsPerChannel(A, n);
   if (!userChannels && ch.channels == 0 && per * C > comm->smCount) {
@@ -464,7 +503,7 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
     if (P == kLL128) sliceBytes = sliceBytes / 240 * 240;  // whole lines and 16-byte slice starts
   }
   sliceBytes = std::max<size_t>(sliceBytes / 16 * 16, 16);
-  const int sliceElems = (int)(sliceBytes / E);
+  const int sliceElems = (int)(sliceBytes / kE);
   // Chunk: VRCCL_STEPS/2 slots (ALLREDUCE_CHUNKSTEPS = NCCL_STEPS/2, Deep
   // Dive (Japanese edition) ch.6). Fewer slots per chunk than the FIFO depth
   // is what keeps the credit ring deadlock-free.
@@ -472,12 +511,12 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
                     : (ch.chunkBytes ? ch.chunkBytes : sliceBytes * (kSteps / 2));
   chunkBytes = std::min(chunkBytes, sliceBytes * (kSteps / 2));
   chunkBytes = std::max<size_t>(chunkBytes / 16 * 16, 16);
-  const int chunkElems = (int)(chunkBytes / E);
+  const int chunkElems = (int)(chunkBytes / kE);
 
   // ---- LL/LL128 flag wrap: clear the FIFO and its counters well before a
   // 32-bit flag could repeat a value still sitting in a slot.
   if (P != kSimple) {
-    const unsigned long long perCh = (bytes + C - 1) / C / E + 1;
+    const unsigned long long perCh = (bytes + C - 1) / C / kE + 1;
     const unsigned long long bound = 2ull * n * ((perCh + sliceElems - 1) / sliceElems + 2ull * n + 2);
     if (comm->llStepBound[P] + bound > (1ull << 31)) {
       const size_t nEdges = size_t(3) * comm->maxChannels * n;
@@ -493,7 +532,8 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
   KArgs ka;
   memset(&ka, 0, sizeof(ka));
   ka.comm = comm->dc;
-  ka.count = count;
+  ka.count = kcount;
+  ka.coll = n == 1 ? kAllReduce : coll;  // one rank: every collective is the copy
   ka.nranks = n;
   ka.nchannels = C;
   ka.chunkElems = chunkElems;
@@ -526,19 +566,37 @@ extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const
   comm->lastAlgo = A;
   comm->lastProto = P;
   comm->lastChannels = C;
-  comm->lastChunk = chunkElems;
-  comm->lastSlice = sliceElems;
+  comm->lastChunk = chunkBytes / E;
+  comm->lastSlice = (int)(sliceBytes / E);
   comm->lastThreads = threads;
   if (comm->debug) {
     char host[64] = {0};
     gethostname(host, sizeof(host) - 1);
     fprintf(stderr,
-            "%s:%d:%ld [%d] VRCCL INFO AllReduce: %zu Bytes -> Algo %s proto %s channel{Lo..Hi}={0..%d} "
+            "%s:%d:%ld [%d] VRCCL INFO %s: %zu Bytes -> Algo %s proto %s channel{Lo..Hi}={0..%d} "
             "chunk %zu slice %d threads %d nranks %d\n",
-            host, (int)getpid(), (long)syscall(SYS_gettid), comm->device, bytes, kAlgoName[A], kProtoName[P],
-            C - 1, chunkBytes, sliceElems, threads, n);
+            host, (int)getpid(), (long)syscall(SYS_gettid), comm->device, kCollName[coll], bytes, kAlgoName[A],
+            kProtoName[P], C - 1, chunkBytes, (int)(sliceBytes / E), threads, n);
   }
   return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const* recvbufs, size_t count,
+                                        vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo,
+                                        vrcclProto_t proto, vrcclComm_t comm, vrcclStream_t stream) {
+  return enqueue(kAllReduce, sendbufs, recvbufs, count, dtype, op, algo, proto, comm, stream);
+}
+
+extern "C" vrcclResult_t vrcclReduceScatter(const void* const* sendbufs, void* const* recvbufs, size_t recvcount,
+                                            vrcclDataType_t dtype, vrcclRedOp_t op, vrcclProto_t proto,
+                                            vrcclComm_t comm, vrcclStream_t stream) {
+  return enqueue(kReduceScatter, sendbufs, recvbufs, recvcount, dtype, op, vrcclAlgoRing, proto, comm, stream);
+}
+
+extern "C" vrcclResult_t vrcclAllGather(const void* const* sendbufs, void* const* recvbufs, size_t sendcount,
+                                        vrcclDataType_t dtype, vrcclProto_t proto, vrcclComm_t comm,
+                                        vrcclStream_t stream) {
+  return enqueue(kAllGather, sendbufs, recvbufs, sendcount, dtype, vrcclSum, vrcclAlgoRing, proto, comm, stream);
 }
 
 extern "C" vrcclResult_t vrcclCommGetLaunchShape(vrcclComm_t comm, int* blocks, int* threads, int* sliceElems) {

@@ -40,6 +40,9 @@ constexpr int kNumProtos = 3;
 
 enum ProtoId { kSimple = 0, kLL = 1, kLL128 = 2 };
 enum AlgoId { kRing = 0, kTree = 1 };
+// What one launch computes: the AllReduce, or one of its two ring phases
+// run alone (ReduceScatter, AllGather).
+enum CollId { kAllReduce = 0, kReduceScatter = 1, kAllGather = 2 };
 
 // FIFO geometry (buffer bytes per slot) and the data one slot carries.
 constexpr size_t kSimpleSlotBytes = 32 * 1024;  // data bytes per Simple slot (max slice)
@@ -93,7 +96,8 @@ struct DevComm {
 
 struct KArgs {
   DevComm comm;
-  unsigned long long count;
+  unsigned long long count;  // AllReduce: elements per rank; phases: elements per block
+  int coll;                  // CollId
   int nranks;
   int nchannels;
   int chunkElems;  // ring chunk K (elements, multiple of 16 bytes)

@@ -33,7 +33,7 @@ PROTO_NAMES = {v: k for k, v in PROTOS.items()}
 ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
 MAX_RANKS = 128
 MAX_CHANNELS = 64
-STEPS = 8
+STEPS = 16
 
 _TORCH_DTYPES = {torch.int32: "int32", torch.float32: "float32", torch.bfloat16: "bfloat16",
                  torch.float16: "float16"}
@@ -43,6 +43,10 @@ _sig = {
     "vrcclCommInit": [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int],
     "vrcclAllReduce": [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p],
+    "vrcclReduceScatter": [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
+                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p],
+    "vrcclAllGather": [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
+                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p],
     "vrcclCommSetSchedule": [ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t],
     "vrcclCommGetLastSchedule": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p, ctypes.POINTER(ctypes.c_size_t)],
     "vrcclCommGetAsyncError": [ctypes.c_void_p, _c_int_p],
@@ -120,6 +124,21 @@ def vrcclAllReduce(sendbufs, recvbufs, count: int, dtype, op, algo="ring", proto
     _check(_lib.vrcclAllReduce(S, R, count, _enum(DTYPES, dtype, "dtype"), _enum(OPS, op, "op"),
                                _enum(ALGOS, algo, "algo"), _enum(PROTOS, proto, "proto"), comm,
                                _stream(stream)), "vrcclAllReduce")
+
+
+def vrcclReduceScatter(sendbufs, recvbufs, recvcount: int, dtype, op, proto="simple", comm=None,
+                       stream=None) -> None:
+    S = (ctypes.c_void_p * len(sendbufs))(*[_ptr(b) for b in sendbufs])
+    R = (ctypes.c_void_p * len(recvbufs))(*[_ptr(b) for b in recvbufs])
+    _check(_lib.vrcclReduceScatter(S, R, recvcount, _enum(DTYPES, dtype, "dtype"), _enum(OPS, op, "op"),
+                                   _enum(PROTOS, proto, "proto"), comm, _stream(stream)), "vrcclReduceScatter")
+
+
+def vrcclAllGather(sendbufs, recvbufs, sendcount: int, dtype, proto="simple", comm=None, stream=None) -> None:
+    S = (ctypes.c_void_p * len(sendbufs))(*[_ptr(b) for b in sendbufs])
+    R = (ctypes.c_void_p * len(recvbufs))(*[_ptr(b) for b in recvbufs])
+    _check(_lib.vrcclAllGather(S, R, sendcount, _enum(DTYPES, dtype, "dtype"), _enum(PROTOS, proto, "proto"), comm,
+                               _stream(stream)), "vrcclAllGather")
 
 
 def vrcclAllReduceNoAlloc(sendbufs, recvbufs, count: int, nranks: int, dtype, op, stream=None) -> None:

@@ -52,6 +52,10 @@ def test_host_side_argument_checks(lib):
     assert lib.vrcclAllReduce(None, None, 1, 0, 0, 0, 0, None, None) == 1
     bogus = ctypes.create_string_buffer(4096)  # not a communicator: the magic check rejects it
     assert lib.vrcclAllReduce(None, None, 1, 0, 0, 0, 0, bogus, None) == 1
+    assert lib.vrcclReduceScatter(None, None, 4, 0, 0, 0, None, None) == 1
+    assert lib.vrcclAllGather(None, None, 4, 0, 0, None, None) == 1
+    assert lib.vrcclReduceScatter(None, None, 4, 0, 0, 0, bogus, None) == 1
+    assert lib.vrcclAllGather(None, None, 4, 0, 0, bogus, None) == 1
     assert lib.vrcclCommDestroy(None) == 0
     assert lib.vrcclCommDestroy(bogus) == 1
     assert lib.vrcclCommAbort(bogus) == 1
@@ -87,3 +91,34 @@ def test_shipped_tuning_table_parses():
         n, algo, proto, ch, lg, sl = map(int, r[:6])
         assert n == 8 and algo in (0, 1) and proto in (0, 1, 2) and 1 <= ch <= 64 and 0 <= lg < 40 and sl > 0
         assert float(r[6]) > 0
+
+
+def test_binding_constants_match_the_header():
+    """The Python binding's copies of the header's macros and enums agree."""
+    pytest.importorskip("torch")
+    from ring_allreduce_reduction_gb300 import build
+    build.build()
+    from ring_allreduce_reduction_gb300 import vrccl
+    txt = open(HEADER).read()
+    macro = {m: int(v) for m, v in re.findall(r"#define\s+(VRCCL_\w+)\s+(\d+)", txt)}
+    assert vrccl.MAX_RANKS == macro["VRCCL_MAX_RANKS"]
+    assert vrccl.MAX_CHANNELS == macro["VRCCL_MAX_CHANNELS"]
+    assert vrccl.STEPS == macro["VRCCL_STEPS"]
+
+    def enum_body(first):
+        body = re.search(r"typedef enum\s*\{([^}]*" + first + r"[^}]*)\}", txt).group(1)
+        body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+        names, val = [], -1
+        for item in [x.strip() for x in body.split(",") if x.strip()]:
+            name, _, rhs = item.partition("=")
+            val = int(rhs) if rhs.strip() else val + 1
+            names.append((name.strip(), val))
+        return dict(names)
+
+    dt = enum_body("vrcclInt32")
+    assert {k: dt["vrccl" + {"int32": "Int32", "float32": "Float32", "bfloat16": "Bfloat16",
+                             "float16": "Float16"}[k]] for k in vrccl.DTYPES} == vrccl.DTYPES
+    ops = enum_body("vrcclSum")
+    assert {k: ops["vrccl" + k.capitalize()] for k in vrccl.OPS} == vrccl.OPS
+    res = enum_body("vrcclSuccess")
+    assert [res[name] for name in vrccl.RESULTS] == list(range(len(vrccl.RESULTS)))
