@@ -97,13 +97,14 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ring_simple_n8_fp32_256MiB.md"
 
 
 def kernel_sources_sha256() -> str:
-    """Hash of the device-side sources (kernel translation units, device
-    headers, the shared layout header): ties an ncu summary to the kernel it
-    measured. Host-only files (the launcher, the tuner) do not enter."""
+    """Hash of the sources the profiled kernel (the Simple-protocol ring) is
+    compiled from: its translation unit, the device headers and the shared
+    layout header. It ties an ncu summary to the kernel it measured; host
+    code and the other kernels' translation units do not enter."""
     import hashlib
     h = hashlib.sha256()
     for f in sorted(os.listdir(KERNEL_SOURCES)):
-        if f.endswith(".cuh") or (f.startswith("kernels_") and f.endswith(".cu")) or f == "vrccl_internal.h":
+        if f.endswith(".cuh") or f == "kernels_simple.cu" or f == "vrccl_internal.h":
             with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
@@ -199,7 +200,7 @@ def cpu_baseline(x: np.ndarray, dtype: str, op: str, nch: int, chunk_elems: int,
                  coll: str = "allreduce") -> dict:
     """The oracle as it stands on the bench's own inputs, replaying the
     schedule the GPU ran (same channels and chunk), repeated until about
-    `min_seconds` of CPU time (at most 5 runs)."""
+    `min_seconds` of CPU time (at most 40 runs)."""
     from oracle import phases, ring as oring
     n, count = x.shape
     run = {"allreduce": lambda: oring.ring_allreduce(x, op, dtype, nch, chunk_elems),
@@ -210,7 +211,7 @@ def cpu_baseline(x: np.ndarray, dtype: str, op: str, nch: int, chunk_elems: int,
         t0 = time.perf_counter()
         run()
         times.append(time.perf_counter() - t0)
-        if sum(times) >= min_seconds or len(times) >= 5:
+        if sum(times) >= min_seconds or len(times) >= 40:
             break
     dt = statistics.mean(times)
     S = count * ELEM[dtype] * (n if coll == "all_gather" else 1)
@@ -280,6 +281,9 @@ def main() -> int:
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     ap.add_argument("--coll", default="allreduce", choices=["allreduce", "reduce_scatter", "all_gather"],
                     help="allreduce (the workload), or one of its two ring phases run alone")
+    ap.add_argument("--algo", default="ring", choices=["ring", "tree", "oneshot"],
+                    help="allreduce only: the schedule timed (the workload's is the ring)")
+    ap.add_argument("--no-bound", action="store_true", help="skip timing the one-shot bound beside the ring")
     ap.add_argument("--bytes-per-rank", type=int, default=0,
                     help="profiling only: a smaller per-rank size than the workload's (reported in config)")
     args = ap.parse_args()
@@ -306,6 +310,9 @@ def main() -> int:
     coll = args.coll
     if coll != "allreduce":
         W["name"] = W["name"].replace("_sum_", "_sum_" + coll + "_")
+    elif args.algo != "ring":
+        W["algo"] = args.algo
+        W["name"] = W["name"].replace("_ring_", "_" + args.algo + "_")
     if args.bytes_per_rank:
         W["bytes_per_rank"] = args.bytes_per_rank
         W["name"] += f" (profiling size {args.bytes_per_rank} B/rank)"
@@ -397,6 +404,29 @@ def main() -> int:
                "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
                "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": round(e2e_ms, 3)}
 
+    # ---- the one-shot bound on the same buffers and schedule: every input
+    # read once, every output written once, the ring's association order
+    bound = None
+    if coll == "allreduce" and W["algo"] == "ring" and not args.no_bound:
+        v.vrcclCommSetSchedule(comm, sched["nchannels"], sched["chunk_elems"] * ELEM[dtype])
+        for _ in range(3):
+            v.vrcclAllReduce(sp, rp, count, dtype, W["op"], "oneshot", "simple", comm, stream)
+        nb = max(3, min(args.steps, 50))
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        b0.record(stream)
+        for _ in range(nb):
+            v.vrcclAllReduce(sp, rp, count, dtype, W["op"], "oneshot", "simple", comm, stream)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bms = b0.elapsed_time(b1) / nb
+        v.vrcclCommSetSchedule(comm, 0, 0)
+        bach = 2 * n * S / (bms / 1e3) / 1e9
+        bound = {"algo": "oneshot", "ms_per_step": round(bms, 4), "achieved": round(bach, 1), "unit": "GB/s",
+                 "frac": round(bach / peak, 4), "ring_time_over_bound": round(ms_step / bms, 3),
+                 "launches": nb + 3}
+
     v.vrcclCommDestroy(comm)
     if rank != 0:
         return 0
@@ -415,6 +445,7 @@ def main() -> int:
                    "l2": "inputs larger than L2 (n*S = 2 GiB in, 2 GiB out); no flush",
                    "algbw_gbs": round(S / (ms_step / 1e3) / 1e9 * world, 3)},
         "roofline": roofline,
+        "oneshot_bound": bound,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,

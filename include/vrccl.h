@@ -106,11 +106,16 @@ typedef enum {
   vrcclNumOps = 5
 } vrcclRedOp_t;
 
-/* Schedules [Architecture §7.1]. */
+/* Schedules [Architecture §7.1]. vrcclAlgoOneShot is not on the pages: an
+ * AllReduce that reads all n inputs of an element at once and writes all n
+ * outputs (no FIFO), in the ring's association order for the ring's channel
+ * count and chunk. It moves only the essential bytes and serves as the HBM
+ * bound the ring is measured against; "auto" never picks it. */
 typedef enum {
   vrcclAlgoRing = 0,
   vrcclAlgoTree = 1,
-  vrcclAlgoAuto = 2
+  vrcclAlgoAuto = 2,
+  vrcclAlgoOneShot = 3
 } vrcclAlgo_t;
 
 /* Wire protocols [Architecture §7.2; Deep Dive §2.4]. */
@@ -138,8 +143,8 @@ typedef enum {
  * default 2000), VRCCL_DEBUG=INFO (prints each call's decision line),
  * VRCCL_PROTO / VRCCL_ALGO (simple|ll|ll128 / ring|tree: what "auto"
  * resolves to), VRCCL_NCHANNELS (channel count "auto" uses),
- * VRCCL_SLICE_BYTES (largest Simple FIFO slot to use, bytes; default 16384,
- * at most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent,
+ * VRCCL_SLICE_BYTES (largest Simple FIFO slot to use, bytes; default and
+ * most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent,
  * default 8), VRCCL_PREFETCH (input slices a Simple agent pulls into L2
  * ahead of use, default 0 = off, at most 32), VRCCL_TUNE_FILE (a measured
  * tuning table, see vrcclCommLoadTuning; without it the table shipped next
@@ -162,7 +167,9 @@ vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchannels);
  *   count     elements per rank. 0 -> success, nothing launched
  *             [Deep Dive (Japanese edition) ch.6, taskAppend step 4].
  *   dtype, op as above.
- *   algo      ring, tree, or auto (the tuning table's choice).
+ *   algo      ring, tree, auto (the tuning table's choice among ring and
+ *             tree), or one-shot (same bits as the ring with the same
+ *             channel count and chunk; `proto` is then ignored).
  *   proto     simple, ll, ll128, or auto (the tuning table's choice).
  *   comm      a live communicator.
  *   stream    cudaStream_t on the communicator's device.

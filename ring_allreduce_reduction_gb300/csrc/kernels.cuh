@@ -35,8 +35,23 @@ __device__ __forceinline__ void channelRange(unsigned long long count, int C, in
 // The loop covers n*K elements; a shorter remainder uses chunks of
 // alignUp(ceil(rem/n), 16 bytes). A chunk moves as slices of at most
 // sliceElems elements, one FIFO step each.
+// One ring agent's slice sequence through its protocol.
+template <int PROTO, int DT, int OP, class It>
+__device__ __forceinline__ void ringAgent(const KArgs& a, Agent& ag, It& it, const char* in, char* out) {
+  using S = typename Ty<DT>::S;
+  constexpr long long E = sizeof(S);
+  if constexpr (PROTO == kSimple) {
+    simplePipeline<DT, OP, false>(a, ag, it, in, out);
+  } else {
+    SliceDesc d;
+    while (it.next(d))
+      if (!runSlice<PROTO, DT, OP, false>(a, ag, in + d.inPos * E, out + d.outPos * E, d.nelem, d.flags)) return;
+    ag.finish(a.comm);
+  }
+}
+
 template <int PROTO, int DT, int OP>
-__global__ void __launch_bounds__(1024) ringKernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(maxAgentThreads(PROTO)) ringKernel(const __grid_constant__ KArgs a) {
   using S = typename Ty<DT>::S;
   constexpr long long E = sizeof(S);
   const int n = a.nranks;
@@ -44,7 +59,8 @@ __global__ void __launch_bounds__(1024) ringKernel(const __grid_constant__ KArgs
   const DevComm& c = a.comm;
   if (aborted(c)) return;
   // AllReduce: channels split the buffer; the phases: channels split a
-  // block, and every loop visits the same range of each block.
+  // block, and every loop visits the same range of each block. A launch
+  // runs one of the two slice sequences.
   unsigned long long lo, hi;
   channelRange<S>(a.count, a.nchannels, ch, lo, hi);
   const char* in = reinterpret_cast<const char*>(a.send[r]);
@@ -56,16 +72,15 @@ __global__ void __launch_bounds__(1024) ringKernel(const __grid_constant__ KArgs
     ag.addRecv(c, ringEdge(ch, (r - 1 + n) % n, n));
     ag.addSend(c, ringEdge(ch, r, n));
   }
-  RingIter it;
-  it.init(n, r, a.coll, (long long)lo, (long long)(hi - lo), (long long)a.count, a.chunkElems, 16 / E,
-          a.sliceElems);
-  if constexpr (PROTO == kSimple) {
-    simplePipeline<DT, OP, false>(a, ag, it, in, out);
+  if (a.coll == kAllReduce || n == 1) {
+    RingIter it;
+    it.init(n, r, (long long)lo, (long long)(hi - lo), a.chunkElems, 16 / E, a.sliceElems);
+    ringAgent<PROTO, DT, OP>(a, ag, it, in, out);
   } else {
-    SliceDesc d;
-    while (it.next(d))
-      if (!runSlice<PROTO, DT, OP, false>(a, ag, in + d.inPos * E, out + d.outPos * E, d.nelem, d.flags)) return;
-    ag.finish(c);
+    PhaseIter it;
+    it.init(n, r, a.coll == kAllGather, (long long)lo, (long long)(hi - lo), (long long)a.count, a.chunkElems,
+            a.sliceElems);
+    ringAgent<PROTO, DT, OP>(a, ag, it, in, out);
   }
 }
 
@@ -135,7 +150,7 @@ __host__ __device__ inline int channelTree(int ch, int C) { return ch < (C + 1) 
 // Root: same, then post-op, write the result and send it down. Down agent:
 // receive from the parent, write the result, forward to the children.
 template <int PROTO, int DT, int OP>
-__global__ void __launch_bounds__(1024) treeKernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(maxAgentThreads(PROTO)) treeKernel(const __grid_constant__ KArgs a) {
   using S = typename Ty<DT>::S;
   constexpr long long E = sizeof(S);
   const int n = a.nranks;

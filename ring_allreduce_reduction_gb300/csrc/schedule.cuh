@@ -27,90 +27,56 @@ struct SliceDesc {
 // A loop covers n*K elements; a shorter remainder uses chunks of
 // alignUp(ceil(rem/n), 16 bytes). A chunk is cut into slices of at most
 // `slice` elements, one FIFO step each. With n == 1 the sequence is a copy.
-//
-// The two phases run alone ("NCCL Source Code Deep Dive", §2.3 walks the
-// AllReduce as a reduce-scatter phase and an all-gather phase of n-1 steps
-// each) use the same chunk order on blocks instead of loop chunks. The
-// channel range [lo, lo + chCount) is then a range within a block of `blk`
-// elements, a loop takes K elements of every block, and chunk c of a loop
-// lives in block c:
-//   ReduceScatter  p = 0 send c = r-1; p = 1..n-2 recvReduceSend c = r-1-p;
-//                  p = n-1 recvReduceCopy (post-op) c = r -> recv buffer
-//   AllGather      p = 0 copySend c = r (own send buffer -> block r);
-//                  p = 1..n-2 recvCopySend c = r-p; p = n-1 recv c = r+1
+// Positions are element offsets from the start of the rank's buffers; the
+// channel's range starts at `lo`.
 struct RingIter {
-  int n, r, coll;
-  long long chCount, K, A, slice, lo, blk;
-  long long off, rem, k;                // loop offset and remainder; chunk size of the loop
-  long long inBase, outBase, len, s;    // current chunk: slices [s, len) from the two bases
-  int p, nprim, flags;
+  int n, r;
+  long long lo, chCount, K, A, slice;
+  long long off, rem, k, s, cHi;
+  int p, flags;
   bool started;
 
-  __device__ __forceinline__ void init(int n_, int r_, int coll_, long long lo_, long long chCount_, long long blk_,
-                                       long long K_, long long A_, long long slice_) {
+  __device__ __forceinline__ void init(int n_, int r_, long long lo_, long long chCount_, long long K_, long long A_,
+                                       long long slice_) {
     n = n_;
     r = r_;
-    coll = coll_;
     lo = lo_;
     chCount = chCount_;
-    blk = blk_;
     K = K_;
     A = A_;
     slice = slice_;
-    nprim = coll == kAllReduce ? 2 * n - 1 : n;
     started = false;
-    s = len = 0;
-    inBase = outBase = 0;
+    s = cHi = 0;
     p = 0;
     off = 0;
     flags = 0;
   }
-  __device__ __forceinline__ static int mod(int x, int m) { return ((x % m) + m) % m; }
   __device__ __forceinline__ void setChunk() {
     int c;
-    if (coll == kAllReduce) {
-      if (p == 0) {
-        c = mod(r - 1, n);
-        flags = F_IN | F_SEND;
-      } else if (p <= n - 2) {
-        c = mod(r - 1 - p, n);
-        flags = F_IN | F_RECV | F_SEND;
-      } else if (p == n - 1) {
-        c = r;
-        flags = F_IN | F_RECV | F_POST | F_OUT | F_SEND;
-      } else if (p <= 2 * n - 3) {
-        c = mod(r - (p - n + 1), n);
-        flags = F_RECV | F_OUT | F_SEND;
-      } else {
-        c = mod(r + 1, n);
-        flags = F_RECV | F_OUT;
-      }
-      const long long cLo = min(rem, (long long)c * k);
-      len = min(rem, (long long)(c + 1) * k) - cLo;
-      inBase = outBase = lo + off + cLo;
-    } else if (coll == kReduceScatter) {
-      c = p == n - 1 ? r : mod(r - 1 - p, n);
-      flags = p == 0 ? (F_IN | F_SEND) : p < n - 1 ? (F_IN | F_RECV | F_SEND) : (F_IN | F_RECV | F_POST | F_OUT);
-      len = k;
-      inBase = (long long)c * blk + lo + off;
-      outBase = lo + off;
+    if (p == 0) {
+      c = (r - 1 + n) % n;
+      flags = F_IN | F_SEND;
+    } else if (p <= n - 2) {
+      c = ((r - 1 - p) % n + n) % n;
+      flags = F_IN | F_RECV | F_SEND;
+    } else if (p == n - 1) {
+      c = r;
+      flags = F_IN | F_RECV | F_POST | F_OUT | F_SEND;
+    } else if (p <= 2 * n - 3) {
+      c = ((r - (p - n + 1)) % n + n) % n;
+      flags = F_RECV | F_OUT | F_SEND;
     } else {
-      c = mod(r - p, n);
-      flags = p == 0 ? (F_IN | F_OUT | F_SEND) : p < n - 1 ? (F_RECV | F_OUT | F_SEND) : (F_RECV | F_OUT);
-      len = k;
-      inBase = lo + off;
-      outBase = (long long)c * blk + lo + off;
+      c = (r + 1) % n;
+      flags = F_RECV | F_OUT;
     }
-    s = 0;
+    const long long cLo = min(rem, (long long)c * k);
+    cHi = off + min(rem, (long long)(c + 1) * k);
+    s = off + cLo;
   }
   __device__ __forceinline__ void setLoop() {
     rem = chCount - off;
-    if (coll == kAllReduce) {
-      const long long loop = (long long)n * K;
-      k = rem >= loop ? K : ((rem + n - 1) / n + A - 1) / A * A;
-    } else {
-      k = min(rem, K);
-    }
+    const long long loop = (long long)n * K;
+    k = rem >= loop ? K : ((rem + n - 1) / n + A - 1) / A * A;
   }
   __device__ __forceinline__ bool next(SliceDesc& d) {
     if (n == 1) {  // single rank: the local copy
@@ -126,6 +92,81 @@ struct RingIter {
       return true;
     }
     while (true) {
+      if (s < cHi) {
+        d.inPos = d.outPos = lo + s;
+        d.nelem = (int)min(slice, cHi - s);
+        d.flags = flags;
+        s += slice;
+        return true;
+      }
+      if (!started) {
+        started = true;
+        if (chCount <= 0) return false;
+        off = 0;
+        p = 0;
+        setLoop();
+      } else if (++p == 2 * n - 1) {
+        off += (long long)n * K;
+        if (off >= chCount) return false;
+        p = 0;
+        setLoop();
+      }
+      setChunk();
+    }
+  }
+};
+
+// The two phases run alone ("NCCL Source Code Deep Dive", §2.3 walks the
+// AllReduce as a reduce-scatter phase and an all-gather phase of n-1 steps
+// each) use the ring's chunk order on blocks instead of loop chunks. The
+// channel range [lo, lo + chCount) is a range within a block of `blk`
+// elements; a loop takes K elements of every block, and chunk c of a loop
+// lives in block c:
+//   ReduceScatter  p = 0 send c = r-1; p = 1..n-2 recvReduceSend c = r-1-p;
+//                  p = n-1 recvReduceCopy (post-op) c = r -> recv buffer
+//   AllGather      p = 0 copySend c = r (own send buffer -> block r);
+//                  p = 1..n-2 recvCopySend c = r-p; p = n-1 recv c = r+1
+// (n > 1; one rank runs the AllReduce copy instead).
+struct PhaseIter {
+  int n, r;
+  bool gather;
+  long long lo, chCount, blk, K, slice;
+  long long off, len, inBase, outBase, s;
+  int p, flags;
+  bool started;
+
+  __device__ __forceinline__ void init(int n_, int r_, bool gather_, long long lo_, long long chCount_,
+                                       long long blk_, long long K_, long long slice_) {
+    n = n_;
+    r = r_;
+    gather = gather_;
+    lo = lo_;
+    chCount = chCount_;
+    blk = blk_;
+    K = K_;
+    slice = slice_;
+    started = false;
+    off = len = inBase = outBase = s = 0;
+    p = 0;
+    flags = 0;
+  }
+  __device__ __forceinline__ void setChunk() {
+    int c;
+    if (!gather) {
+      c = p == n - 1 ? r : ((r - 1 - p) % n + n) % n;
+      flags = p == 0 ? (F_IN | F_SEND) : p < n - 1 ? (F_IN | F_RECV | F_SEND) : (F_IN | F_RECV | F_POST | F_OUT);
+      inBase = (long long)c * blk + lo + off;
+      outBase = lo + off;
+    } else {
+      c = ((r - p) % n + n) % n;
+      flags = p == 0 ? (F_IN | F_OUT | F_SEND) : p < n - 1 ? (F_RECV | F_OUT | F_SEND) : (F_RECV | F_OUT);
+      inBase = lo + off;
+      outBase = (long long)c * blk + lo + off;
+    }
+    s = 0;
+  }
+  __device__ __forceinline__ bool next(SliceDesc& d) {
+    while (true) {
       if (s < len) {
         d.inPos = inBase + s;
         d.outPos = outBase + s;
@@ -139,13 +180,12 @@ struct RingIter {
         if (chCount <= 0) return false;
         off = 0;
         p = 0;
-        setLoop();
-      } else if (++p == nprim) {
-        off += coll == kAllReduce ? (long long)n * K : K;
+      } else if (++p == n) {
+        off += K;
         if (off >= chCount) return false;
         p = 0;
-        setLoop();
       }
+      len = min(chCount - off, K);
       setChunk();
     }
   }

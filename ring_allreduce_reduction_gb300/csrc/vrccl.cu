@@ -29,6 +29,7 @@ extern const void* const kRingLL[4][5];
 extern const void* const kTreeLL[4][5];
 extern const void* const kRingLL128[4][5];
 extern const void* const kTreeLL128[4][5];
+extern const void* const kOneShot[4][5];
 
 const void* kernelFor(int algo, int proto, int dtype, int op) {
   if (dtype < 0 || dtype >= 4 || op < 0 || op >= 5) return nullptr;
@@ -72,7 +73,7 @@ struct vrcclComm {
   bool haveLast;
   int lastAlgo, lastProto, lastChannels;
   size_t lastChunk;
-  int lastSlice, lastThreads;
+  int lastSlice, lastThreads, lastBlocks;
   // LL / LL128 flags are the low bits of a growing step count: an upper
   // bound of the steps issued so far decides when to clear the FIFOs.
   unsigned long long llStepBound[kNumProtos];
@@ -108,7 +109,7 @@ static int parseAlgo(const char* v) {
   return -1;
 }
 
-static const char* kAlgoName[2] = {"Ring", "Tree"};
+static const char* kAlgoName[4] = {"Ring", "Tree", "Auto", "OneShot"};
 static const char* kProtoName[3] = {"Simple", "LL", "LL128"};
 static const size_t kElemSize[4] = {4, 4, 2, 2};
 
@@ -396,6 +397,62 @@ static bool overlapFree(int coll, const void* const* s, void* const* r, int n, s
 
 static const char* kCollName[3] = {"AllReduce", "ReduceScatter", "AllGather"};
 
+// The one-shot AllReduce: C and the chunk as the ring/Simple schedule has
+// them (before any co-residency shrink, which the one-shot does not need),
+// then one plain launch of a grid that fills every SM.
+static vrcclResult_t launchOneShot(vrcclComm_t comm, const void* const* sendbufs, void* const* recvbufs,
+                                   size_t count, int dtype, int op, int C, const Choice& ch, vrcclStream_t stream) {
+  const int n = comm->nranks;
+  const size_t E = kElemSize[dtype];
+  const size_t slice = std::max<size_t>(std::min(comm->envSliceBytes ? comm->envSliceBytes
+                                                 : ch.sliceBytes     ? ch.sliceBytes
+                                                                     : kSimpleSlotBytes,
+                                                 kSimpleSlotBytes) / 16 * 16, 16);
+  size_t chunkBytes = comm->forceChunkBytes ? comm->forceChunkBytes
+                    : (ch.chunkBytes ? ch.chunkBytes : slice * (kSteps / 2));
+  chunkBytes = std::min(chunkBytes, slice * (kSteps / 2));
+  chunkBytes = std::max<size_t>(chunkBytes / 16 * 16, 16);
+  const void* fn = kOneShot[dtype][op];
+  const int threads = 512;
+  const int perSm = residentCapacity(comm, fn, threads, 0) / std::max(1, comm->smCount);
+  if (perSm < 1) return vrcclInternalError;
+  KArgs ka;
+  memset(&ka, 0, sizeof(ka));
+  ka.comm = comm->dc;
+  ka.count = count;
+  ka.coll = kAllReduce;
+  ka.nranks = n;
+  ka.nchannels = C;
+  ka.chunkElems = (int)(chunkBytes / E);
+  ka.sliceElems = (int)(slice / E);
+  ka.scale = 1.0f / (float)n;
+  for (int r = 0; r < n; ++r) {
+    ka.send[r] = sendbufs[r];
+    ka.recv[r] = recvbufs[r];
+  }
+  const unsigned long long tiles = (count / (16 / E) + threads * 4 - 1) / (threads * 4);
+  const unsigned grid = (unsigned)std::max<unsigned long long>(1, std::min<unsigned long long>(tiles,
+                                                                   (unsigned long long)perSm * comm->smCount));
+  void* args[] = {&ka};
+  cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(threads), args, 0, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return vrcclCudaError;
+  }
+  comm->haveLast = true;
+  comm->lastAlgo = vrcclAlgoOneShot;
+  comm->lastProto = kSimple;
+  comm->lastChannels = C;
+  comm->lastChunk = chunkBytes / E;
+  comm->lastSlice = (int)(slice / E);
+  comm->lastThreads = threads;
+  comm->lastBlocks = (int)grid;
+  if (comm->debug)
+    fprintf(stderr, "[%d] VRCCL INFO AllReduce: %zu Bytes -> Algo OneShot (ring order channel{Lo..Hi}={0..%d} "
+            "chunk %zu) grid %u threads %d nranks %d\n", comm->device, count * E, C - 1, chunkBytes, grid, threads, n);
+  return vrcclSuccess;
+}
+
 // One collective call: validate, choose the schedule, launch once.
 //   coll   AllReduce: count = elements per rank. ReduceScatter / AllGather:
 //          count = elements per block (recvcount / sendcount).
@@ -406,9 +463,10 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
   // Deep Dive (Japanese edition) ch.6).
   if (!validComm(comm)) return vrcclInvalidArgument;
   if ((unsigned)dtype >= (unsigned)vrcclNumTypes || (unsigned)op >= (unsigned)vrcclNumOps ||
-      (unsigned)algo > (unsigned)vrcclAlgoAuto || (unsigned)proto > (unsigned)vrcclProtoAuto)
+      (unsigned)algo > (unsigned)vrcclAlgoOneShot || (unsigned)proto > (unsigned)vrcclProtoAuto)
     return vrcclInvalidArgument;
   if (!sendbufs || !recvbufs) return vrcclInvalidArgument;
+  if (coll != kAllReduce && algo != vrcclAlgoRing) return vrcclInvalidArgument;
   const int n = comm->nranks;
   for (int r = 0; r < n; ++r) {
     if (!sendbufs[r] || !recvbufs[r]) return vrcclInvalidArgument;
@@ -446,9 +504,12 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
   // bytes = one rank's send (AllReduce, ReduceScatter) or recv (AllGather)
   // buffer; the phases take the ring's entries of the table at that size.
   const size_t bytes = coll == kAllReduce ? blockBytes : blockBytes * n;
+  // The one-shot takes the ring/Simple schedule's channel count and chunk,
+  // which fix its association order.
+  const bool oneShot = algo == vrcclAlgoOneShot;
   const bool userAlgo = coll == kAllReduce && algo != vrcclAlgoAuto, userProto = proto != vrcclProtoAuto;
-  const int fixA = coll != kAllReduce ? kRing : userAlgo ? (int)algo : comm->envAlgo;
-  const int fixP = userProto ? (int)proto : comm->envProto;
+  const int fixA = coll != kAllReduce || oneShot ? kRing : userAlgo ? (int)algo : comm->envAlgo;
+  const int fixP = oneShot ? kSimple : userProto ? (int)proto : comm->envProto;
   Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, n == 1 ? kRing : fixA, fixP);
   int A = fixA >= 0 ? fixA : ch.algo;
   int P = fixP >= 0 ? fixP : ch.proto;
@@ -468,6 +529,7 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
     const int k = per * C / comm->smCount;
     C = std::max(1, k * comm->smCount / per);
   }
+  if (oneShot) return launchOneShot(comm, sendbufs, recvbufs, count, dtype, op, C, ch, stream);
   int threads = 256, stages = 0;
   size_t smem = 0;
   size_t sliceBytes = slotDataBytes(P);
@@ -569,6 +631,7 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
   comm->lastChunk = chunkBytes / E;
   comm->lastSlice = (int)(sliceBytes / E);
   comm->lastThreads = threads;
+  comm->lastBlocks = per * C;
   if (comm->debug) {
     char host[64] = {0};
     gethostname(host, sizeof(host) - 1);
@@ -602,7 +665,7 @@ extern "C" vrcclResult_t vrcclAllGather(const void* const* sendbufs, void* const
 extern "C" vrcclResult_t vrcclCommGetLaunchShape(vrcclComm_t comm, int* blocks, int* threads, int* sliceElems) {
   if (!validComm(comm)) return vrcclInvalidArgument;
   if (!comm->haveLast) return vrcclInvalidUsage;
-  if (blocks) *blocks = agentsPerChannel(comm->lastAlgo, comm->nranks) * comm->lastChannels;
+  if (blocks) *blocks = comm->lastBlocks;
   if (threads) *threads = comm->lastThreads;
   if (sliceElems) *sliceElems = comm->lastSlice;
   return vrcclSuccess;

@@ -50,7 +50,12 @@ constexpr int kLLSlotLines = 1024;              // 16-byte lines: 8 data bytes e
 constexpr int kLL128SlotLines = 256;            // 128-byte lines: 120 data bytes each
 constexpr int kLL128DataBytes = 120;
 constexpr int kMaxStages = 8;          // Simple pipeline depth in shared memory
-constexpr int kMaxConsumerWarps = 29;  // Simple: 3 service warps + up to 29 consumer warps
+constexpr int kMaxConsumerWarps = 16;  // Simple: 3 service warps + up to 16 consumer warps
+// Thread bound a kernel is compiled for. A Simple agent has at most 3 + 16
+// warps (608 threads); its bound of 736 threads caps registers at 65536 / 736
+// = 89 per thread, so two 352-thread agents (8 consumer warps) still fit on
+// one SM without spilling. LL / LL128 agents use up to 1024 threads.
+__host__ __device__ constexpr int maxAgentThreads(int proto) { return proto == 0 ? 736 : 1024; }
 constexpr int kMaxPrefetch = 32;       // Simple: largest input L2 prefetch distance (slices)
 
 __host__ __device__ constexpr size_t slotBufferBytes(int proto) {

@@ -26,7 +26,7 @@ RESULTS = ["vrcclSuccess", "vrcclInvalidArgument", "vrcclInvalidUsage", "vrcclIn
            "vrcclCudaError", "vrcclTimeout", "vrcclAborted"]
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2, "float16": 3}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
-ALGOS = {"ring": 0, "tree": 1, "auto": 2}
+ALGOS = {"ring": 0, "tree": 1, "auto": 2, "oneshot": 3}
 PROTOS = {"simple": 0, "ll": 1, "ll128": 2, "auto": 3}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 PROTO_NAMES = {v: k for k, v in PROTOS.items()}
