@@ -269,6 +269,105 @@ def run_reference(args) -> int:
     return 0
 
 
+BUCKET = {"nranks": 8, "dtype": "bfloat16", "bytes_per_rank": 1 << 30, "ntensors": 224, "lo": 4 << 10,
+          "hi": 64 << 20, "op": "avg", "max_channels": 32}
+
+
+def run_bucket(args) -> int:
+    """The gradient bucket: n = 8, 1 GiB of bf16 per rank made of 224
+    tensors of log-uniform sizes in [4 KiB, 64 MiB], op avg, algo and
+    protocol auto; one step reduces the whole bucket, as one flat call
+    (`flat`), as 224 calls in one group (`group`) or as 224 separate calls
+    (`separate`)."""
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from ring_allreduce_reduction_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from ring_allreduce_reduction_gb300 import vrccl as v
+    from ring_allreduce_reduction_gb300.workloads import bucket_sizes, make_inputs
+    B = BUCKET
+    n, S = B["nranks"], B["bytes_per_rank"]
+    sizes = bucket_sizes(S, B["ntensors"], B["lo"], B["hi"], seed=0, align=16)
+    offs = np.concatenate([[0], np.cumsum(sizes)]) // 2
+    x = make_inputs(n, S // 2, "bfloat16", "normal", seed=rank_seed(rank), std=1e-3)
+    send = torch.from_numpy(x.view(np.int16)).cuda()
+    recv = torch.empty_like(send)
+    comm = v.vrcclCommInit(n, B["max_channels"])
+    stream = torch.cuda.current_stream()
+    views = [([send[r, int(a):int(b)] for r in range(n)], [recv[r, int(a):int(b)] for r in range(n)], int(b - a))
+             for a, b in zip(offs[:-1], offs[1:])]
+
+    def step():
+        if args.bucket == "flat":
+            v.vrcclAllReduce([send[r] for r in range(n)], [recv[r] for r in range(n)], S // 2, "bfloat16",
+                             B["op"], "auto", "auto", comm, stream)
+            return
+        if args.bucket == "group":
+            v.vrcclGroupStart()
+        for sp, rp, cnt in views:
+            v.vrcclAllReduce(sp, rp, cnt, "bfloat16", B["op"], "auto", "auto", comm, stream)
+        if args.bucket == "group":
+            v.vrcclGroupEnd()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if args.bucket == "flat":
+        launches = 1
+    elif args.bucket == "group":
+        launches = 1 + max(v.vrcclCommGetGroupSchedule(comm, t)["launch"] for t in range(len(views)))
+    else:
+        launches = len(views)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    err = v.vrcclCommGetAsyncError(comm)
+    if err:
+        raise RuntimeError(f"device error in the timed region: {v.RESULTS[err]}")
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, "cuda")
+    value = busbw_gbs(S, n, ms / 1e3) * world
+    peak, peak_kind = measured_peak()
+    achieved = 2 * n * S / (ms / 1e3) / 1e9
+    v.vrcclCommDestroy(comm)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": f"allreduce busbw (n=8 virtual ranks, bf16 1 GiB/rank bucket of 224 tensors, avg, auto; "
+                  f"{args.bucket})",
+        "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"n8_bf16_avg_bucket224_1GiB_{args.bucket}", "nranks": n, "bytes_per_rank": S,
+                   "tensors": len(views), "launches_per_step": launches,
+                   "l2": "inputs larger than L2 (8 GiB in, 8 GiB out); no flush"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                     "algorithmic_bytes_per_step": 2 * n * S, "note": "whole step, all launches"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -284,6 +383,8 @@ def main() -> int:
     ap.add_argument("--algo", default="ring", choices=["ring", "tree", "oneshot"],
                     help="allreduce only: the schedule timed (the workload's is the ring)")
     ap.add_argument("--no-bound", action="store_true", help="skip timing the one-shot bound beside the ring")
+    ap.add_argument("--bucket", default="", choices=["", "flat", "group", "separate"],
+                    help="time the 224-tensor bf16 gradient bucket instead of the workload")
     ap.add_argument("--bytes-per-rank", type=int, default=0,
                     help="profiling only: a smaller per-rank size than the workload's (reported in config)")
     args = ap.parse_args()
@@ -291,6 +392,8 @@ def main() -> int:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.bucket:
+        return run_bucket(args)
 
     import torch
     world, rank, local = dist_env()

@@ -164,7 +164,8 @@ vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchannels);
  *   recvbufs  host array of n device pointers; recvbufs[r] receives
  *             `count` elements. recvbufs[r] == sendbufs[r] (in place) is
  *             allowed; any other overlap between the 2n buffers is not.
- *   count     elements per rank. 0 -> success, nothing launched
+ *   count     elements per rank. 0 -> success, nothing launched, and the
+ *             buffer pointers are not examined (they may be NULL)
  *             [Deep Dive (Japanese edition) ch.6, taskAppend step 4].
  *   dtype, op as above.
  *   algo      ring, tree, auto (the tuning table's choice among ring and
@@ -201,7 +202,8 @@ vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const* recvbufs,
  *             recvbufs[r] == sendbufs[r] + r*recvcount elements.
  *   recvcount elements per block; recvcount * element size must be a
  *             multiple of 16 bytes when n > 1, so that every block starts
- *             on a 16-byte boundary. 0 -> success, nothing launched.
+ *             on a 16-byte boundary. 0 -> success, nothing launched, the
+ *             pointers not examined.
  *   dtype, op as for vrcclAllReduce (avg: the same pre-scale / post-op).
  *   proto     simple, ll, ll128, or auto. The schedule is the ring.
  * Channels split each block; a loop takes one chunk of every block. Errors
@@ -231,6 +233,45 @@ vrcclResult_t vrcclReduceScatter(const void* const* sendbufs, void* const* recvb
 vrcclResult_t vrcclAllGather(const void* const* sendbufs, void* const* recvbufs, size_t sendcount,
                              vrcclDataType_t dtype, vrcclProto_t proto, vrcclComm_t comm,
                              vrcclStream_t stream);
+
+/*
+ * vrcclGroupStart / vrcclGroupEnd -- ncclGroupStart / ncclGroupEnd
+ * [Architecture §9.2, §9.6; Deep Dive (Japanese edition) ch.5]. Between
+ * the two, vrcclAllReduce / vrcclReduceScatter / vrcclAllGather check their
+ * arguments (and return any error at once) but only register the call; the
+ * outermost vrcclGroupEnd schedules every registered call of every
+ * communicator and enqueues it. Groups nest; the depth is per thread.
+ * Scheduling, per communicator: AllReduces of one type, op and requested
+ * protocol whose algo is ring or auto are sorted by size, largest first,
+ * and cut into runs of sizes within 4x of the run's largest
+ * (ncclPrepareTasks). A run is scheduled as a whole, by the tuning table at
+ * its total size, and enqueued as one launch of the grouped ring kernel
+ * (more launches if its pointers exceed the kernel's parameter space);
+ * each of its calls gets the channel count a call of its own size would
+ * get. Every other call is enqueued alone. The calls of one group are not
+ * ordered among themselves: none may touch a buffer another one writes.
+ * All of a group's calls on one communicator must use one stream
+ * (vrcclInvalidUsage otherwise, at the call). vrcclGroupEnd returns the
+ * first error of a launch and drops the calls not yet enqueued; without a
+ * matching vrcclGroupStart it returns vrcclInvalidUsage. Like every call
+ * here, it only enqueues: synchronise the stream before reading results.
+ * vrcclAllReduceNoAlloc is never grouped.
+ */
+vrcclResult_t vrcclGroupStart(void);
+vrcclResult_t vrcclGroupEnd(void);
+
+/*
+ * vrcclCommGetGroupSchedule -- what ran for call `index` (0-based, in call
+ * order) of the communicator's most recent group: algorithm, protocol,
+ * channel count, chunk (elements; together with the channel count it
+ * fixes the association order of every float result), and the launch
+ * (0-based, in enqueue order within the group) that carried it. Calls that
+ * shared a launch report the same launch.
+ * Errors: vrcclInvalidArgument (bad handle, index out of range);
+ * vrcclInvalidUsage (nothing ran for that call: count 0).
+ */
+vrcclResult_t vrcclCommGetGroupSchedule(vrcclComm_t comm, int index, int* algo, int* proto, int* nchannels,
+                                        size_t* chunkElems, int* launch);
 
 /*
  * vrcclCommSetSchedule -- pin the channel count and chunk size used by

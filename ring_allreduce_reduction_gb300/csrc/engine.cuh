@@ -195,8 +195,8 @@ __device__ __forceinline__ void storeUnit(char* p, uint2 v, int validBytes) {
 // on the line until both flags equal the expected step; the line's data is
 // then complete (the two halves were written by one 16-byte store). Flags
 // only grow, so slots are never cleared.
-template <int DT, int OP, bool TREE>
-__device__ bool llSlice(const KArgs& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
+template <int DT, int OP, bool TREE, class Args>
+__device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
   using S = typename Ty<DT>::S;
   __shared__ int smFail;
   const DevComm& c = a.comm;
@@ -271,8 +271,8 @@ __device__ bool llSlice(const KArgs& a, Agent& ag, const char* in, char* out, in
 // the other lanes' data stores before it, and the reader's flag lane polls
 // with acquire loads and the warp barrier orders the data loads after it.
 // The line format and its 93.75 % payload are unchanged.
-template <int DT, int OP, bool TREE>
-__device__ bool llSlice128(const KArgs& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
+template <int DT, int OP, bool TREE, class Args>
+__device__ bool llSlice128(const Args& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
   using S = typename Ty<DT>::S;
   __shared__ int smFail;
   const DevComm& c = a.comm;
@@ -373,8 +373,8 @@ __device__ bool llSlice128(const KArgs& a, Agent& ag, const char* in, char* out,
   return true;
 }
 
-template <int PROTO, int DT, int OP, bool TREE>
-__device__ __forceinline__ bool runSlice(const KArgs& a, Agent& ag, const char* in, char* out, int nelem,
+template <int PROTO, int DT, int OP, bool TREE, class Args>
+__device__ __forceinline__ bool runSlice(const Args& a, Agent& ag, const char* in, char* out, int nelem,
                                          int flags) {
   if constexpr (PROTO == kLL) return llSlice<DT, OP, TREE>(a, ag, in, out, nelem, flags);
   if constexpr (PROTO == kLL128) return llSlice128<DT, OP, TREE>(a, ag, in, out, nelem, flags);

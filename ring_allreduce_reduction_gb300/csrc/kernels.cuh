@@ -36,8 +36,8 @@ __device__ __forceinline__ void channelRange(unsigned long long count, int C, in
 // alignUp(ceil(rem/n), 16 bytes). A chunk moves as slices of at most
 // sliceElems elements, one FIFO step each.
 // One ring agent's slice sequence through its protocol.
-template <int PROTO, int DT, int OP, class It>
-__device__ __forceinline__ void ringAgent(const KArgs& a, Agent& ag, It& it, const char* in, char* out) {
+template <int PROTO, int DT, int OP, class Args, class It>
+__device__ __forceinline__ void ringAgent(const Args& a, Agent& ag, It& it, const char* in, char* out) {
   using S = typename Ty<DT>::S;
   constexpr long long E = sizeof(S);
   if constexpr (PROTO == kSimple) {

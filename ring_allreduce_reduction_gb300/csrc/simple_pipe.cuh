@@ -77,8 +77,8 @@ __device__ __forceinline__ void drainStages(const DevComm& c, unsigned long long
   }
 }
 
-template <int DT, int OP, bool TREE, class It>
-__device__ void simplePipeline(const KArgs& a, Agent& ag, It it, const char* in, char* out) {
+template <int DT, int OP, bool TREE, class Args, class It>
+__device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, char* out) {
   using S = typename Ty<DT>::S;
   constexpr int E = sizeof(S);
   constexpr int V = 16 / E;

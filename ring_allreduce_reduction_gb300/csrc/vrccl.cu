@@ -30,6 +30,19 @@ extern const void* const kTreeLL[4][5];
 extern const void* const kRingLL128[4][5];
 extern const void* const kTreeLL128[4][5];
 extern const void* const kOneShot[4][5];
+extern const void* const kGroupSimple[4][5];
+extern const void* const kGroupLL[4][5];
+extern const void* const kGroupLL128[4][5];
+
+const void* groupKernelFor(int proto, int dtype, int op) {
+  if (dtype < 0 || dtype >= 4 || op < 0 || op >= 5) return nullptr;
+  switch (proto) {
+    case kSimple: return kGroupSimple[dtype][op];
+    case kLL: return kGroupLL[dtype][op];
+    case kLL128: return kGroupLL128[dtype][op];
+  }
+  return nullptr;
+}
 
 const void* kernelFor(int algo, int proto, int dtype, int op) {
   if (dtype < 0 || dtype >= 4 || op < 0 || op >= 5) return nullptr;
@@ -48,6 +61,22 @@ const void* kernelFor(int algo, int proto, int dtype, int op) {
 // Sentinels at both ends of the communicator, as ncclComm's startMagic /
 // endMagic (Deep Dive §2.1): a stale or foreign handle fails the check.
 static constexpr uint64_t kMagic = 0x5652434331474233ull;  // "VRCC1GB3"
+
+// A validated collective call. AllReduce: count = elements per rank.
+// ReduceScatter / AllGather: count = elements per block.
+struct Call {
+  int coll, dtype, op, algo, proto;
+  size_t count;
+  std::vector<const void*> send;
+  std::vector<void*> recv;
+  vrcclStream_t stream;
+};
+
+struct GroupSched {
+  int algo, proto, channels;
+  size_t chunk;
+  int launch;  // order of the launch that ran the call within its group
+};
 
 struct vrcclComm {
   uint64_t startMagic;
@@ -78,8 +107,14 @@ struct vrcclComm {
   // bound of the steps issued so far decides when to clear the FIFOs.
   unsigned long long llStepBound[kNumProtos];
   Tuner tuner;
+  std::vector<Call> pending;            // calls registered inside a group
+  std::vector<GroupSched> groupSched;   // per call of the last group: what ran
+  int groupLaunches;                    // launches made by the last group
   uint64_t endMagic;
 };
+
+static std::mutex gLiveMu;
+static std::vector<vrcclComm*> gLive;  // communicators not yet destroyed
 
 static bool validComm(const vrcclComm* c) {
   return c && c->startMagic == kMagic && c->endMagic == kMagic;
@@ -131,6 +166,10 @@ extern "C" const char* vrcclGetErrorString(vrcclResult_t r) {
 }
 
 static void freeComm(vrcclComm* c) {
+  {
+    std::lock_guard<std::mutex> lk(gLiveMu);
+    gLive.erase(std::remove(gLive.begin(), gLive.end(), c), gLive.end());
+  }
   for (int p = 0; p < kNumProtos; ++p)
     if (c->fifoAlloc[p]) cudaFree(c->fifoAlloc[p]);
   if (c->ctrlAlloc) cudaFree(c->ctrlAlloc);
@@ -151,6 +190,8 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
   vrcclComm* c = new vrcclComm();
   memset(static_cast<void*>(c), 0, sizeof(*c));
   new (&c->tuner) Tuner();
+  new (&c->pending) std::vector<Call>();
+  new (&c->groupSched) std::vector<GroupSched>();
   c->startMagic = c->endMagic = kMagic;
   c->device = dev;
   c->nranks = nranks;
@@ -202,6 +243,10 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
   c->envWarps = std::max(0, envInt("VRCCL_SIMPLE_WARPS", 0));
   c->envPrefetch = std::min(kMaxPrefetch, std::max(0, envInt("VRCCL_PREFETCH", 0)));
   c->tuner.loadEnvFile(nranks);
+  {
+    std::lock_guard<std::mutex> lk(gLiveMu);
+    gLive.push_back(c);
+  }
   *comm = c;
   return vrcclSuccess;
 }
@@ -397,76 +442,21 @@ static bool overlapFree(int coll, const void* const* s, void* const* r, int n, s
 
 static const char* kCollName[3] = {"AllReduce", "ReduceScatter", "AllGather"};
 
-// The one-shot AllReduce: C and the chunk as the ring/Simple schedule has
-// them (before any co-residency shrink, which the one-shot does not need),
-// then one plain launch of a grid that fills every SM.
-static vrcclResult_t launchOneShot(vrcclComm_t comm, const void* const* sendbufs, void* const* recvbufs,
-                                   size_t count, int dtype, int op, int C, const Choice& ch, vrcclStream_t stream) {
-  const int n = comm->nranks;
-  const size_t E = kElemSize[dtype];
-  const size_t slice = std::max<size_t>(std::min(comm->envSliceBytes ? comm->envSliceBytes
-                                                 : ch.sliceBytes     ? ch.sliceBytes
-                                                                     : kSimpleSlotBytes,
-                                                 kSimpleSlotBytes) / 16 * 16, 16);
-  size_t chunkBytes = comm->forceChunkBytes ? comm->forceChunkBytes
-                    : (ch.chunkBytes ? ch.chunkBytes : slice * (kSteps / 2));
-  chunkBytes = std::min(chunkBytes, slice * (kSteps / 2));
-  chunkBytes = std::max<size_t>(chunkBytes / 16 * 16, 16);
-  const void* fn = kOneShot[dtype][op];
-  const int threads = 512;
-  const int perSm = residentCapacity(comm, fn, threads, 0) / std::max(1, comm->smCount);
-  if (perSm < 1) return vrcclInternalError;
-  KArgs ka;
-  memset(&ka, 0, sizeof(ka));
-  ka.comm = comm->dc;
-  ka.count = count;
-  ka.coll = kAllReduce;
-  ka.nranks = n;
-  ka.nchannels = C;
-  ka.chunkElems = (int)(chunkBytes / E);
-  ka.sliceElems = (int)(slice / E);
-  ka.scale = 1.0f / (float)n;
-  for (int r = 0; r < n; ++r) {
-    ka.send[r] = sendbufs[r];
-    ka.recv[r] = recvbufs[r];
-  }
-  const unsigned long long tiles = (count / (16 / E) + threads * 4 - 1) / (threads * 4);
-  const unsigned grid = (unsigned)std::max<unsigned long long>(1, std::min<unsigned long long>(tiles,
-                                                                   (unsigned long long)perSm * comm->smCount));
-  void* args[] = {&ka};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(threads), args, 0, (cudaStream_t)stream);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return vrcclCudaError;
-  }
-  comm->haveLast = true;
-  comm->lastAlgo = vrcclAlgoOneShot;
-  comm->lastProto = kSimple;
-  comm->lastChannels = C;
-  comm->lastChunk = chunkBytes / E;
-  comm->lastSlice = (int)(slice / E);
-  comm->lastThreads = threads;
-  comm->lastBlocks = (int)grid;
-  if (comm->debug)
-    fprintf(stderr, "[%d] VRCCL INFO AllReduce: %zu Bytes -> Algo OneShot (ring order channel{Lo..Hi}={0..%d} "
-            "chunk %zu) grid %u threads %d nranks %d\n", comm->device, count * E, C - 1, chunkBytes, grid, threads, n);
-  return vrcclSuccess;
-}
+// ------------------------------------------------------------- one call
 
-// One collective call: validate, choose the schedule, launch once.
-//   coll   AllReduce: count = elements per rank. ReduceScatter / AllGather:
-//          count = elements per block (recvcount / sendcount).
-static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const* recvbufs, size_t count,
-                             vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo, vrcclProto_t proto,
-                             vrcclComm_t comm, vrcclStream_t stream) {
-  // Argument checks first (ncclEnqueueCheck: CommCheck, then ArgsCheck,
-  // Deep Dive (Japanese edition) ch.6).
+// Argument checks (ncclEnqueueCheck: CommCheck, then ArgsCheck, Deep Dive
+// (Japanese edition) ch.6).
+static vrcclResult_t checkCall(vrcclComm_t comm, int coll, const void* const* sendbufs, void* const* recvbufs,
+                               size_t count, vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo,
+                               vrcclProto_t proto) {
   if (!validComm(comm)) return vrcclInvalidArgument;
   if ((unsigned)dtype >= (unsigned)vrcclNumTypes || (unsigned)op >= (unsigned)vrcclNumOps ||
       (unsigned)algo > (unsigned)vrcclAlgoOneShot || (unsigned)proto > (unsigned)vrcclProtoAuto)
     return vrcclInvalidArgument;
-  if (!sendbufs || !recvbufs) return vrcclInvalidArgument;
   if (coll != kAllReduce && algo != vrcclAlgoRing) return vrcclInvalidArgument;
+  if (comm->failed || comm->aborted) return vrcclInvalidUsage;
+  if (count == 0) return vrcclSuccess;  // touches nothing: the pointers are not examined
+  if (!sendbufs || !recvbufs) return vrcclInvalidArgument;
   const int n = comm->nranks;
   for (int r = 0; r < n; ++r) {
     if (!sendbufs[r] || !recvbufs[r]) return vrcclInvalidArgument;
@@ -481,36 +471,35 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
   const size_t sendBytes = coll == kReduceScatter ? blockBytes * n : blockBytes;
   const size_t recvBytes = coll == kAllGather ? blockBytes * n : blockBytes;
   if (!overlapFree(coll, sendbufs, recvbufs, n, sendBytes, recvBytes)) return vrcclInvalidArgument;
-  if (comm->failed || comm->aborted) return vrcclInvalidUsage;
-  if (count == 0) return vrcclSuccess;  // taskAppend step 4: nothing to do
-
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev != comm->device) return vrcclInvalidUsage;
+  return vrcclSuccess;
+}
 
-  // The all-gather phase only copies: it runs as 4-byte words, whatever
-  // the type (the blocks are whole 16-byte units).
-  int kdtype = dtype, kop = op;
-  size_t kcount = count, kE = E;
-  if (coll == kAllGather) {
-    kdtype = vrcclInt32;
-    kop = vrcclSum;
-    kcount = n > 1 ? blockBytes / 4 : count;
-    kE = n > 1 ? 4 : E;
-    if (n == 1) kdtype = dtype;  // a single rank is a plain copy in the user's type
-  }
+// The launch shape of one ring/tree launch.
+struct Shape {
+  int A, P, C;
+  int threads, stages;
+  size_t smem, sliceBytes, chunkBytes;
+  const void* fn;
+  int per;  // agents per channel
+};
 
-  // ---- schedule: algo, proto, channels, chunk, slice, threads
-  // bytes = one rank's send (AllReduce, ReduceScatter) or recv (AllGather)
-  // buffer; the phases take the ring's entries of the table at that size.
-  const size_t bytes = coll == kAllReduce ? blockBytes : blockBytes * n;
-  // The one-shot takes the ring/Simple schedule's channel count and chunk,
-  // which fix its association order.
-  const bool oneShot = algo == vrcclAlgoOneShot;
-  const bool userAlgo = coll == kAllReduce && algo != vrcclAlgoAuto, userProto = proto != vrcclProtoAuto;
-  const int fixA = coll != kAllReduce || oneShot ? kRing : userAlgo ? (int)algo : comm->envAlgo;
-  const int fixP = oneShot ? kSimple : userProto ? (int)proto : comm->envProto;
+// Chooses algorithm, protocol and channels for `bytes` per rank (the tuning
+// table, or what the caller / environment forced), then the largest agent
+// shape with which every agent of the launch is resident at once (all
+// agents wait on each other). grouped: the kernel is the grouped ring.
+static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto, size_t bytes, int kdtype, int kop,
+                                 size_t kE, bool grouped, Shape* out, Choice* tuned = nullptr) {
+  const int n = comm->nranks;
+  const bool userAlgo = coll == kAllReduce && algo != vrcclAlgoAuto && !grouped;
+  const bool userProto = proto != vrcclProtoAuto;
+  const int fixA = (coll != kAllReduce || grouped || algo == vrcclAlgoOneShot) ? kRing
+                 : userAlgo ? algo : comm->envAlgo;
+  const int fixP = algo == vrcclAlgoOneShot ? kSimple : userProto ? proto : comm->envProto;
   Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, n == 1 ? kRing : fixA, fixP);
+  if (tuned) *tuned = ch;
   int A = fixA >= 0 ? fixA : ch.algo;
   int P = fixP >= 0 ? fixP : ch.proto;
   if (n == 1) A = kRing;  // a single rank is a local copy (ncclLaunchOneRank)
@@ -519,8 +508,7 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
         : (ch.channels > 0 ? std::min(ch.channels, comm->maxChannels)
                            : defaultChannels(P, bytes, n, comm->maxChannels));
   const bool userChannels = comm->forceChannels || comm->envChannels;
-
-  const void* fn = kernelFor(A, P, kdtype, kop);
+  const void* fn = grouped ? groupKernelFor(P, kdtype, kop) : kernelFor(A, P, kdtype, kop);
   if (!fn) return vrcclInternalError;
   const int per = agentsPerChannel(A, n);
   if (!userChannels && ch.channels == 0 && per * C > comm->smCount) {
@@ -529,87 +517,91 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
     const int k = per * C / comm->smCount;
     C = std::max(1, k * comm->smCount / per);
   }
-  if (oneShot) return launchOneShot(comm, sendbufs, recvbufs, count, dtype, op, C, ch, stream);
-  int threads = 256, stages = 0;
-  size_t smem = 0;
-  size_t sliceBytes = slotDataBytes(P);
-  if (P == kSimple) {
-    // All agents of a launch wait on each other: they must all be resident.
+  Shape s;
+  s.A = A;
+  s.P = P;
+  s.fn = fn;
+  s.per = per;
+  s.threads = 256;
+  s.stages = 0;
+  s.smem = 0;
+  s.sliceBytes = slotDataBytes(P);
+  const size_t wantSlice = std::min(comm->envSliceBytes ? comm->envSliceBytes
+                                    : ch.sliceBytes     ? ch.sliceBytes
+                                                        : kSimpleSlotBytes,
+                                    kSimpleSlotBytes);
+  if (algo == vrcclAlgoOneShot) {
+    s.sliceBytes = wantSlice;  // no agents: only C and the chunk matter
+  } else if (P == kSimple) {
     // Shrink the agent first, then (if the caller left it open) the channels.
     const int nbuf = A == kTree ? 3 : 2;
-    const size_t want = std::min(comm->envSliceBytes ? comm->envSliceBytes
-                                 : ch.sliceBytes     ? ch.sliceBytes
-                                                     : kSimpleSlotBytes,
-                                 kSimpleSlotBytes);
     SimpleShape sh;
-    const int maxWarps = comm->envWarps ? comm->envWarps : 8;
-    while (!pickSimpleShape(comm, fn, per * C, nbuf, want, maxWarps, &sh)) {
+    const int maxWarps = comm->envWarps ? std::min(comm->envWarps, kMaxConsumerWarps) : 8;
+    while (!pickSimpleShape(comm, fn, per * C, nbuf, wantSlice, maxWarps, &sh)) {
       if (userChannels || C == 1) return userAlgo || userChannels ? vrcclInvalidUsage : vrcclInternalError;
       --C;
     }
-    threads = sh.threads;
-    stages = sh.stages;
-    smem = sh.smem;
-    sliceBytes = sh.sliceBytes;
+    s.threads = sh.threads;
+    s.stages = sh.stages;
+    s.smem = sh.smem;
+    s.sliceBytes = sh.sliceBytes;
   } else {
-    int cap = residentCapacity(comm, fn, threads, 0);
-    while (cap < per * C && threads > 64) {
-      threads /= 2;
-      cap = residentCapacity(comm, fn, threads, 0);
+    int cap = residentCapacity(comm, fn, s.threads, 0);
+    while (cap < per * C && s.threads > 64) {
+      s.threads /= 2;
+      cap = residentCapacity(comm, fn, s.threads, 0);
     }
     if (cap < per * C) {
       if (userChannels) return vrcclInvalidUsage;
       C = cap / per;
       if (C < 1) return userAlgo ? vrcclInvalidUsage : vrcclInternalError;
     }
-    if (P == kLL128) sliceBytes = sliceBytes / 240 * 240;  // whole lines and 16-byte slice starts
+    if (P == kLL128) s.sliceBytes = s.sliceBytes / 240 * 240;  // whole lines and 16-byte slice starts
   }
-  sliceBytes = std::max<size_t>(sliceBytes / 16 * 16, 16);
-  const int sliceElems = (int)(sliceBytes / kE);
+  s.C = C;
+  s.sliceBytes = std::max<size_t>(s.sliceBytes / 16 * 16, 16);
   // Chunk: VRCCL_STEPS/2 slots (ALLREDUCE_CHUNKSTEPS = NCCL_STEPS/2, Deep
   // Dive (Japanese edition) ch.6). Fewer slots per chunk than the FIFO depth
   // is what keeps the credit ring deadlock-free.
   size_t chunkBytes = comm->forceChunkBytes ? comm->forceChunkBytes
-                    : (ch.chunkBytes ? ch.chunkBytes : sliceBytes * (kSteps / 2));
-  chunkBytes = std::min(chunkBytes, sliceBytes * (kSteps / 2));
-  chunkBytes = std::max<size_t>(chunkBytes / 16 * 16, 16);
-  const int chunkElems = (int)(chunkBytes / kE);
+                    : (ch.chunkBytes ? ch.chunkBytes : s.sliceBytes * (kSteps / 2));
+  chunkBytes = std::min(chunkBytes, s.sliceBytes * (kSteps / 2));
+  s.chunkBytes = std::max<size_t>(chunkBytes / 16 * 16, 16);
+  (void)kE;
+  *out = s;
+  return vrcclSuccess;
+}
 
-  // ---- LL/LL128 flag wrap: clear the FIFO and its counters well before a
-  // 32-bit flag could repeat a value still sitting in a slot.
-  if (P != kSimple) {
-    const unsigned long long perCh = (bytes + C - 1) / C / kE + 1;
-    const unsigned long long bound = 2ull * n * ((perCh + sliceElems - 1) / sliceElems + 2ull * n + 2);
-    if (comm->llStepBound[P] + bound > (1ull << 31)) {
-      const size_t nEdges = size_t(3) * comm->maxChannels * n;
-      if (cudaMemsetAsync(comm->fifoAlloc[P], 0, fifoBytes(P, n, comm->maxChannels), (cudaStream_t)stream) !=
-              cudaSuccess ||
-          cudaMemsetAsync(comm->dc.ctrl[P], 0, nEdges * sizeof(EdgeCtrl), (cudaStream_t)stream) != cudaSuccess)
-        return vrcclCudaError;
-      comm->llStepBound[P] = 0;
-    }
-    comm->llStepBound[P] += bound;
+// LL / LL128 flags are the low 32 bits of each edge's step count: before a
+// launch that may take up to `steps` more steps per edge, clear the FIFO and
+// its counters if a flag value could repeat one still sitting in a slot.
+static vrcclResult_t llReserve(vrcclComm_t comm, int P, unsigned long long steps, vrcclStream_t stream) {
+  if (P == kSimple) return vrcclSuccess;
+  const int n = comm->nranks;
+  if (comm->llStepBound[P] + steps > (1ull << 31)) {
+    const size_t nEdges = size_t(3) * comm->maxChannels * n;
+    if (cudaMemsetAsync(comm->fifoAlloc[P], 0, fifoBytes(P, n, comm->maxChannels), (cudaStream_t)stream) !=
+            cudaSuccess ||
+        cudaMemsetAsync(comm->dc.ctrl[P], 0, nEdges * sizeof(EdgeCtrl), (cudaStream_t)stream) != cudaSuccess)
+      return vrcclCudaError;
+    comm->llStepBound[P] = 0;
   }
+  comm->llStepBound[P] += steps;
+  return vrcclSuccess;
+}
 
-  KArgs ka;
-  memset(&ka, 0, sizeof(ka));
-  ka.comm = comm->dc;
-  ka.count = kcount;
-  ka.coll = n == 1 ? kAllReduce : coll;  // one rank: every collective is the copy
-  ka.nranks = n;
-  ka.nchannels = C;
-  ka.chunkElems = chunkElems;
-  ka.sliceElems = sliceElems;
-  ka.scale = 1.0f / (float)n;
-  ka.stages = stages;
-  ka.prefetch = P == kSimple ? comm->envPrefetch : 0;
-  for (int r = 0; r < n; ++r) {
-    ka.send[r] = sendbufs[r];
-    ka.recv[r] = recvbufs[r];
-  }
+// Upper bound of the FIFO steps one edge takes for `elems` elements over C
+// channels in slices of `sliceElems`.
+static unsigned long long stepBound(int n, unsigned long long elems, int C, int sliceElems) {
+  const unsigned long long perCh = (elems + C - 1) / C + 1;
+  return 2ull * n * ((perCh + sliceElems - 1) / sliceElems + 2ull * n + 2);
+}
+
+static vrcclResult_t cooperativeLaunch(const void* fn, int blocks, int threads, size_t smem, void* arg,
+                                       vrcclStream_t stream) {
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)(per * C));
+  cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = (cudaStream_t)stream;
@@ -618,30 +610,327 @@ static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const*
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {&ka};
+  void* args[] = {arg};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? vrcclInvalidUsage : vrcclCudaError;
   }
-  comm->haveLast = true;
-  comm->lastAlgo = A;
-  comm->lastProto = P;
-  comm->lastChannels = C;
-  comm->lastChunk = chunkBytes / E;
-  comm->lastSlice = (int)(sliceBytes / E);
-  comm->lastThreads = threads;
-  comm->lastBlocks = per * C;
-  if (comm->debug) {
-    char host[64] = {0};
-    gethostname(host, sizeof(host) - 1);
-    fprintf(stderr,
-            "%s:%d:%ld [%d] VRCCL INFO %s: %zu Bytes -> Algo %s proto %s channel{Lo..Hi}={0..%d} "
-            "chunk %zu slice %d threads %d nranks %d\n",
-            host, (int)getpid(), (long)syscall(SYS_gettid), comm->device, kCollName[coll], bytes, kAlgoName[A],
-            kProtoName[P], C - 1, chunkBytes, (int)(sliceBytes / E), threads, n);
-  }
   return vrcclSuccess;
+}
+
+static void recordLast(vrcclComm_t comm, int algo, const Shape& s, size_t E, int blocks) {
+  comm->haveLast = true;
+  comm->lastAlgo = algo;
+  comm->lastProto = s.P;
+  comm->lastChannels = s.C;
+  comm->lastChunk = s.chunkBytes / E;
+  comm->lastSlice = (int)(s.sliceBytes / E);
+  comm->lastThreads = s.threads;
+  comm->lastBlocks = blocks;
+}
+
+static void debugLine(vrcclComm_t comm, const char* what, size_t bytes, const char* algoName, const Shape& s,
+                      int blocks) {
+  if (!comm->debug) return;
+  char host[64] = {0};
+  gethostname(host, sizeof(host) - 1);
+  fprintf(stderr,
+          "%s:%d:%ld [%d] VRCCL INFO %s: %zu Bytes -> Algo %s proto %s channel{Lo..Hi}={0..%d} "
+          "chunk %zu slice %zu threads %d blocks %d nranks %d\n",
+          host, (int)getpid(), (long)syscall(SYS_gettid), comm->device, what, bytes, algoName, kProtoName[s.P],
+          s.C - 1, s.chunkBytes, s.sliceBytes, s.threads, blocks, comm->nranks);
+}
+
+// The one-shot AllReduce: C and the chunk as the ring/Simple schedule has
+// them (before any co-residency shrink, which the one-shot does not need),
+// then one plain launch of a grid that fills every SM.
+static vrcclResult_t launchOneShot(vrcclComm_t comm, const Call& k, const Shape& s) {
+  const int n = comm->nranks;
+  const size_t E = kElemSize[k.dtype];
+  const void* fn = kOneShot[k.dtype][k.op];
+  const int threads = 512;
+  const int perSm = residentCapacity(comm, fn, threads, 0) / std::max(1, comm->smCount);
+  if (perSm < 1) return vrcclInternalError;
+  KArgs ka;
+  memset(&ka, 0, sizeof(ka));
+  ka.comm = comm->dc;
+  ka.count = k.count;
+  ka.coll = kAllReduce;
+  ka.nranks = n;
+  ka.nchannels = s.C;
+  ka.chunkElems = (int)(s.chunkBytes / E);
+  ka.sliceElems = (int)(s.sliceBytes / E);
+  ka.scale = 1.0f / (float)n;
+  for (int r = 0; r < n; ++r) {
+    ka.send[r] = k.send[r];
+    ka.recv[r] = k.recv[r];
+  }
+  const unsigned long long tiles = (k.count / (16 / E) + threads * 4 - 1) / (threads * 4);
+  const unsigned grid = (unsigned)std::max<unsigned long long>(1, std::min<unsigned long long>(tiles,
+                                                                   (unsigned long long)perSm * comm->smCount));
+  void* args[] = {&ka};
+  cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(threads), args, 0, (cudaStream_t)k.stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return vrcclCudaError;
+  }
+  Shape r = s;
+  r.threads = threads;
+  r.P = kSimple;
+  recordLast(comm, vrcclAlgoOneShot, r, E, (int)grid);
+  debugLine(comm, "AllReduce", k.count * E, "OneShot", r, (int)grid);
+  return vrcclSuccess;
+}
+
+// Runs one validated call as one launch.
+static vrcclResult_t runCall(vrcclComm_t comm, const Call& k) {
+  const int n = comm->nranks;
+  const size_t E = kElemSize[k.dtype];
+  if (k.count == 0) return vrcclSuccess;  // taskAppend step 4: nothing to do
+  // The all-gather phase only copies: it runs as 4-byte words, whatever
+  // the type (the blocks are whole 16-byte units).
+  int kdtype = k.dtype, kop = k.op;
+  size_t kcount = k.count, kE = E;
+  if (k.coll == kAllGather && n > 1) {
+    kdtype = vrcclInt32;
+    kop = vrcclSum;
+    kcount = k.count * E / 4;
+    kE = 4;
+  }
+  // bytes = one rank's send (AllReduce, ReduceScatter) or recv (AllGather)
+  // buffer; the phases take the ring's entries of the table at that size.
+  const size_t bytes = k.coll == kAllReduce ? k.count * E : k.count * E * n;
+  Shape s;
+  vrcclResult_t res = chooseShape(comm, k.coll, k.algo, k.proto, bytes, kdtype, kop, kE, false, &s);
+  if (res != vrcclSuccess) return res;
+  if (k.algo == vrcclAlgoOneShot) return launchOneShot(comm, k, s);
+  const int sliceElems = (int)(s.sliceBytes / kE);
+  res = llReserve(comm, s.P, stepBound(n, bytes / kE, s.C, sliceElems), k.stream);
+  if (res != vrcclSuccess) return res;
+
+  KArgs ka;
+  memset(&ka, 0, sizeof(ka));
+  ka.comm = comm->dc;
+  ka.count = kcount;
+  ka.coll = n == 1 ? kAllReduce : k.coll;  // one rank: every collective is the copy
+  ka.nranks = n;
+  ka.nchannels = s.C;
+  ka.chunkElems = (int)(s.chunkBytes / kE);
+  ka.sliceElems = sliceElems;
+  ka.scale = 1.0f / (float)n;
+  ka.stages = s.stages;
+  ka.prefetch = s.P == kSimple ? comm->envPrefetch : 0;
+  for (int r = 0; r < n; ++r) {
+    ka.send[r] = k.send[r];
+    ka.recv[r] = k.recv[r];
+  }
+  const int blocks = s.per * s.C;
+  res = cooperativeLaunch(s.fn, blocks, s.threads, s.smem, &ka, k.stream);
+  if (res != vrcclSuccess) return res;
+  recordLast(comm, s.A, s, E, blocks);
+  debugLine(comm, kCollName[k.coll], bytes, kAlgoName[s.A], s, blocks);
+  return vrcclSuccess;
+}
+
+// ----------------------------------------------------------------- groups
+//
+// ncclGroupStart / ncclGroupEnd ("NCCL architecture ...", §9.2 and §9.6;
+// Deep Dive (Japanese edition) ch.5 and ch.6): between the two, calls are
+// checked and only registered; the outermost vrcclGroupEnd schedules what
+// each communicator registered. The group depth is per thread.
+
+static thread_local int tlGroupDepth = 0;
+static thread_local std::vector<vrcclComm*> tlGroupComms;
+
+static bool isLive(vrcclComm* c) {
+  std::lock_guard<std::mutex> lk(gLiveMu);
+  return std::find(gLive.begin(), gLive.end(), c) != gLive.end();
+}
+
+// Grouping: AllReduces of one (type, op, requested protocol) on the ring
+// (algo ring or auto) are bucketed, sorted by size, largest first, and cut
+// into runs whose sizes lie within 4x of the run's largest (ncclPrepareTasks,
+// "NCCL architecture ...", §9.2). A run is scheduled as a whole: the
+// protocol and channel budget come from the tuning table at the run's total
+// size (its launch latency is paid once, which is what numPipeOps expresses
+// in NCCL's model), each task takes the channel count a call of its own
+// size would get, and tasks fill channel ranges round-robin. Every other
+// call runs alone.
+static vrcclResult_t launchRun(vrcclComm_t comm, const std::vector<Call>& calls, const std::vector<int>& run) {
+  const int n = comm->nranks;
+  const Call& k0 = calls[run[0]];
+  const size_t E = kElemSize[k0.dtype];
+  size_t total = 0;
+  for (int i : run) total += calls[i].count * E;
+  Shape s;
+  vrcclResult_t res = chooseShape(comm, kAllReduce, vrcclAlgoRing, k0.proto, total, k0.dtype, k0.op, E, true, &s);
+  if (res != vrcclSuccess) return res;
+  const int sliceElems = (int)(s.sliceBytes / E);
+  const int maxTasks = std::min(kMaxGroupTasks, kGroupPtrs / n);
+  GroupArgs* g = new GroupArgs;
+  size_t i0 = 0;
+  int cursor = 0;
+  while (i0 < run.size() && res == vrcclSuccess) {
+    memset(static_cast<void*>(g), 0, sizeof(*g));
+    g->comm = comm->dc;
+    g->nranks = n;
+    g->nchannels = s.C;
+    g->chunkElems = (int)(s.chunkBytes / E);
+    g->sliceElems = sliceElems;
+    g->stages = s.stages;
+    g->prefetch = s.P == kSimple ? comm->envPrefetch : 0;
+    g->scale = 1.0f / (float)n;
+    unsigned long long steps = 0;
+    size_t bytes = 0;
+    int t = 0;
+    for (; t < maxTasks && i0 + t < run.size(); ++t) {
+      const Call& k = calls[run[i0 + t]];
+      const size_t b = k.count * E;
+      const Choice own = comm->tuner.choose(n, b, comm->maxChannels, kRing, s.P);
+      int nch = comm->forceChannels ? comm->forceChannels
+              : comm->envChannels   ? comm->envChannels
+              : own.channels > 0    ? own.channels
+                                    : defaultChannels(s.P, b, n, comm->maxChannels);
+      nch = std::max(1, std::min(nch, s.C));
+      g->task[t].count = k.count;
+      g->task[t].chLo = cursor;
+      g->task[t].nch = nch;
+      cursor = (cursor + nch) % s.C;
+      for (int r = 0; r < n; ++r) {
+        g->send[t * n + r] = k.send[r];
+        g->recv[t * n + r] = k.recv[r];
+      }
+      steps += stepBound(n, k.count, nch, sliceElems);
+      bytes += b;
+      comm->groupSched[run[i0 + t]] = {kRing, s.P, nch, s.chunkBytes / E, comm->groupLaunches};
+    }
+    g->ntasks = t;
+    res = llReserve(comm, s.P, steps, k0.stream);
+    if (res == vrcclSuccess) res = cooperativeLaunch(s.fn, s.per * s.C, s.threads, s.smem, g, k0.stream);
+    if (res == vrcclSuccess) {
+      ++comm->groupLaunches;
+      recordLast(comm, kRing, s, E, s.per * s.C);
+      debugLine(comm, "AllReduce(group)", bytes, "Ring", s, s.per * s.C);
+    }
+    i0 += t;
+  }
+  delete g;
+  return res;
+}
+
+static vrcclResult_t runGroup(vrcclComm_t comm) {
+  std::vector<Call> calls;
+  calls.swap(comm->pending);
+  comm->groupSched.assign(calls.size(), GroupSched{-1, -1, 0, 0, -1});
+  comm->groupLaunches = 0;
+  vrcclResult_t res = vrcclSuccess;
+  // bucket -> call indices, in call order
+  std::vector<std::pair<long long, std::vector<int>>> buckets;
+  std::vector<int> alone;
+  for (int i = 0; i < (int)calls.size(); ++i) {
+    const Call& k = calls[i];
+    const bool ringable = k.coll == kAllReduce && comm->nranks > 1 && k.count > 0 &&
+                          (k.algo == vrcclAlgoRing || (k.algo == vrcclAlgoAuto && comm->envAlgo != kTree));
+    if (!ringable) {
+      alone.push_back(i);
+      continue;
+    }
+    const long long key = ((long long)k.dtype * vrcclNumOps + k.op) * 8 + k.proto;
+    auto it = std::find_if(buckets.begin(), buckets.end(), [&](const auto& b) { return b.first == key; });
+    if (it == buckets.end()) {
+      buckets.push_back({key, {}});
+      it = buckets.end() - 1;
+    }
+    it->second.push_back(i);
+  }
+  for (auto& b : buckets) {
+    std::vector<int>& v = b.second;
+    std::stable_sort(v.begin(), v.end(), [&](int a, int c) { return calls[a].count > calls[c].count; });
+    size_t i = 0;
+    while (i < v.size() && res == vrcclSuccess) {
+      size_t j = i + 1;
+      while (j < v.size() && calls[v[i]].count < 4 * calls[v[j]].count) ++j;
+      std::vector<int> run(v.begin() + i, v.begin() + j);
+      res = launchRun(comm, calls, run);
+      i = j;
+    }
+  }
+  for (size_t a = 0; a < alone.size() && res == vrcclSuccess; ++a) {
+    const Call& k = calls[alone[a]];
+    res = runCall(comm, k);
+    if (res == vrcclSuccess && k.count > 0)
+      comm->groupSched[alone[a]] = {comm->lastAlgo, comm->lastProto, comm->lastChannels, comm->lastChunk,
+                                    comm->groupLaunches++};
+  }
+  return res;
+}
+
+extern "C" vrcclResult_t vrcclGroupStart(void) {
+  ++tlGroupDepth;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclGroupEnd(void) {
+  if (tlGroupDepth <= 0) return vrcclInvalidUsage;
+  if (--tlGroupDepth > 0) return vrcclSuccess;
+  std::vector<vrcclComm*> comms;
+  comms.swap(tlGroupComms);
+  vrcclResult_t res = vrcclSuccess;
+  for (vrcclComm* c : comms) {
+    if (!isLive(c)) continue;
+    if (res == vrcclSuccess) {
+      res = runGroup(c);
+    } else {
+      c->pending.clear();  // an earlier launch failed: drop the rest of the group
+    }
+  }
+  return res;
+}
+
+extern "C" vrcclResult_t vrcclCommGetGroupSchedule(vrcclComm_t comm, int index, int* algo, int* proto,
+                                                   int* nchannels, size_t* chunkElems, int* launch) {
+  if (!validComm(comm)) return vrcclInvalidArgument;
+  if (index < 0 || index >= (int)comm->groupSched.size()) return vrcclInvalidArgument;
+  const GroupSched& g = comm->groupSched[index];
+  if (g.algo < 0) return vrcclInvalidUsage;  // nothing was launched for that call (count 0)
+  if (algo) *algo = g.algo;
+  if (proto) *proto = g.proto;
+  if (nchannels) *nchannels = g.channels;
+  if (chunkElems) *chunkElems = g.chunk;
+  if (launch) *launch = g.launch;
+  return vrcclSuccess;
+}
+
+// Checks a call, then runs it now or, inside a group, registers it.
+static vrcclResult_t enqueue(int coll, const void* const* sendbufs, void* const* recvbufs, size_t count,
+                             vrcclDataType_t dtype, vrcclRedOp_t op, vrcclAlgo_t algo, vrcclProto_t proto,
+                             vrcclComm_t comm, vrcclStream_t stream) {
+  vrcclResult_t res = checkCall(comm, coll, sendbufs, recvbufs, count, dtype, op, algo, proto);
+  if (res != vrcclSuccess) return res;
+  if (count == 0 && tlGroupDepth == 0) return vrcclSuccess;  // taskAppend step 4: nothing to do
+  Call k;
+  k.coll = coll;
+  k.dtype = dtype;
+  k.op = op;
+  k.algo = algo;
+  k.proto = proto;
+  k.count = count;
+  if (count > 0) {
+    k.send.assign(sendbufs, sendbufs + comm->nranks);
+    k.recv.assign(recvbufs, recvbufs + comm->nranks);
+  }
+  k.stream = stream;
+  if (tlGroupDepth > 0) {
+    // All of a group's calls on one communicator share one stream.
+    if (!comm->pending.empty() && comm->pending[0].stream != stream) return vrcclInvalidUsage;
+    if (comm->pending.empty() &&
+        std::find(tlGroupComms.begin(), tlGroupComms.end(), comm) == tlGroupComms.end())
+      tlGroupComms.push_back(comm);
+    comm->pending.push_back(std::move(k));
+    return vrcclSuccess;
+  }
+  return runCall(comm, k);
 }
 
 extern "C" vrcclResult_t vrcclAllReduce(const void* const* sendbufs, void* const* recvbufs, size_t count,

@@ -114,6 +114,34 @@ struct KArgs {
   void* recv[kMaxRanks];
 };
 
+// A grouped launch: several AllReduces of one type and op, run one after
+// another by every channel they use (ncclGroupStart / ncclGroupEnd put a
+// group's collectives into one plan, one kernel launch, "NCCL architecture
+// ...", §9.6). Task t covers channels chLo .. chLo + nch - 1 (mod
+// nchannels); its rank-r buffers are send[t * nranks + r] and
+// recv[t * nranks + r]. The whole block is a kernel parameter (<= 32 KB).
+constexpr int kMaxGroupTasks = 128;
+constexpr int kGroupPtrs = 1536;  // per side: tasks x ranks of one launch
+struct GroupTask {
+  unsigned long long count;  // elements
+  int chLo, nch;
+};
+struct GroupArgs {
+  DevComm comm;
+  int nranks;
+  int nchannels;   // channels of the launch
+  int chunkElems;  // ring chunk K (elements, multiple of 16 bytes)
+  int sliceElems;  // elements per FIFO step
+  int stages;      // Simple: shared-memory stages
+  int prefetch;    // Simple: input L2 prefetch distance (0 = off)
+  int ntasks;
+  float scale;     // avg pre-scale 1.0f / n
+  GroupTask task[kMaxGroupTasks];
+  const void* send[kGroupPtrs];
+  void* recv[kGroupPtrs];
+};
+static_assert(sizeof(GroupArgs) < 32000, "GroupArgs must fit the kernel parameter space");
+
 __host__ __device__ inline int ringEdge(int ch, int r, int n) { return ch * n + r; }
 __host__ __device__ inline int treeUpEdge(int ch, int c, int n, int maxCh) { return maxCh * n + ch * n + c; }
 __host__ __device__ inline int treeDownEdge(int ch, int c, int n, int maxCh) { return 2 * maxCh * n + ch * n + c; }
@@ -121,5 +149,7 @@ __host__ __device__ inline int treeDownEdge(int ch, int c, int n, int maxCh) { r
 // Kernel table (defined by the kernel translation units).
 // Returns the __global__ function for (algo, proto, dtype, op) or nullptr.
 const void* kernelFor(int algo, int proto, int dtype, int op);
+// The grouped ring kernel for (proto, dtype, op), or nullptr.
+const void* groupKernelFor(int proto, int dtype, int op);
 
 }  // namespace vrccl

@@ -47,6 +47,10 @@ _sig = {
                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p],
     "vrcclAllGather": [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
                        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p],
+    "vrcclGroupStart": [],
+    "vrcclGroupEnd": [],
+    "vrcclCommGetGroupSchedule": [ctypes.c_void_p, ctypes.c_int, _c_int_p, _c_int_p, _c_int_p,
+                                  ctypes.POINTER(ctypes.c_size_t), _c_int_p],
     "vrcclCommSetSchedule": [ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t],
     "vrcclCommGetLastSchedule": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p, ctypes.POINTER(ctypes.c_size_t)],
     "vrcclCommGetAsyncError": [ctypes.c_void_p, _c_int_p],
@@ -147,6 +151,23 @@ def vrcclAllReduceNoAlloc(sendbufs, recvbufs, count: int, nranks: int, dtype, op
     R = (ctypes.c_void_p * len(recvbufs))(*[_ptr(b) for b in recvbufs])
     _check(_lib.vrcclAllReduceNoAlloc(S, R, count, nranks, _enum(DTYPES, dtype, "dtype"), _enum(OPS, op, "op"),
                                       _stream(stream)), "vrcclAllReduceNoAlloc")
+
+
+def vrcclGroupStart() -> None:
+    _check(_lib.vrcclGroupStart(), "vrcclGroupStart")
+
+
+def vrcclGroupEnd() -> None:
+    _check(_lib.vrcclGroupEnd(), "vrcclGroupEnd")
+
+
+def vrcclCommGetGroupSchedule(comm, index: int) -> dict:
+    a, p, c, l = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    k = ctypes.c_size_t()
+    _check(_lib.vrcclCommGetGroupSchedule(comm, index, ctypes.byref(a), ctypes.byref(p), ctypes.byref(c),
+                                          ctypes.byref(k), ctypes.byref(l)), "vrcclCommGetGroupSchedule")
+    return {"algo": ALGO_NAMES[a.value], "proto": PROTO_NAMES[p.value], "nchannels": c.value,
+            "chunk_elems": k.value, "launch": l.value}
 
 
 def vrcclCommSetSchedule(comm, nchannels: int = 0, chunkBytes: int = 0) -> None:

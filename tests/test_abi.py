@@ -122,3 +122,16 @@ def test_binding_constants_match_the_header():
     assert {k: ops["vrccl" + k.capitalize()] for k in vrccl.OPS} == vrccl.OPS
     res = enum_body("vrcclSuccess")
     assert [res[name] for name in vrccl.RESULTS] == list(range(len(vrccl.RESULTS)))
+
+
+def test_group_depth_on_the_host(lib):
+    """Group bookkeeping needs no GPU: an unmatched end is refused, nested
+    empty groups succeed."""
+    assert lib.vrcclGroupEnd() == 2
+    assert lib.vrcclGroupStart() == 0
+    assert lib.vrcclGroupStart() == 0
+    assert lib.vrcclGroupEnd() == 0
+    assert lib.vrcclGroupEnd() == 0
+    assert lib.vrcclGroupEnd() == 2
+    bogus = ctypes.create_string_buffer(4096)
+    assert lib.vrcclCommGetGroupSchedule(bogus, 0, None, None, None, None, None) == 1
