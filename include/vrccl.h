@@ -144,8 +144,8 @@ typedef enum {
  * VRCCL_PROTO / VRCCL_ALGO (simple|ll|ll128 / ring|tree: what "auto"
  * resolves to), VRCCL_NCHANNELS (channel count "auto" uses),
  * VRCCL_SLICE_BYTES (largest Simple FIFO slot to use, bytes; default and
- * most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent,
- * default 8), VRCCL_PREFETCH (input slices a Simple agent pulls into L2
+ * most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent, at
+ * most 16; default 16 for 2-byte types, 8 for 4-byte ones), VRCCL_PREFETCH (input slices a Simple agent pulls into L2
  * ahead of use, default 0 = off, at most 32), VRCCL_TUNE_FILE (a measured
  * tuning table, see vrcclCommLoadTuning; without it the table shipped next
  * to the library, tuning/gb300_n<nranks>.txt, is used when present).

@@ -264,11 +264,31 @@ __device__ __forceinline__ float fromWord(uint32_t w, float*) { return __uint_as
 __device__ __forceinline__ uint32_t toWord(int32_t x) { return uint32_t(x); }
 __device__ __forceinline__ uint32_t toWord(float x) { return __float_as_uint(x); }
 
+// Two 2-byte sums in one instruction. For bf16 and fp16 the binary32 sum
+// of two values of the type is either exact or differs from the exact sum
+// by far less than half a unit of the type, so one correctly rounded
+// (round-to-nearest-even) packed add gives the same bits as "binary32 add,
+// then round to the type".
+__device__ __forceinline__ uint32_t addBf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t addF16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t combineWord(uint32_t a, uint32_t b) {
   using S = typename Ty<DT>::S;
   if constexpr (sizeof(S) == 4) {
     return toWord(combine<DT, OP>(fromWord(a, (S*)nullptr), fromWord(b, (S*)nullptr)));
+  } else if constexpr ((OP == vrcclSum || OP == vrcclAvg) && DT == vrcclBfloat16) {
+    return addBf16x2(a, b);
+  } else if constexpr ((OP == vrcclSum || OP == vrcclAvg) && DT == vrcclFloat16) {
+    return addF16x2(a, b);
   } else {
     uint32_t lo = combine<DT, OP>(S(a & 0xffffu), S(b & 0xffffu));
     uint32_t hi = combine<DT, OP>(S(a >> 16), S(b >> 16));
@@ -283,9 +303,16 @@ __device__ __forceinline__ uint32_t prescaleWord(uint32_t a, float scale) {
   } else if constexpr (sizeof(S) == 4) {
     return toWord(prescale<DT, OP>(fromWord(a, (S*)nullptr), scale));
   } else {
-    uint32_t lo = prescale<DT, OP>(S(a & 0xffffu), scale);
-    uint32_t hi = prescale<DT, OP>(S(a >> 16), scale);
-    return lo | (hi << 16);
+    // binary32 products, then both rounded (to nearest even) by one packed
+    // conversion; the high half of the word is the second element.
+    const float lo = __fmul_rn(Ty<DT>::toF(S(a & 0xffffu)), scale);
+    const float hi = __fmul_rn(Ty<DT>::toF(S(a >> 16)), scale);
+    uint32_t d;
+    if constexpr (DT == vrcclBfloat16)
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    else
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
   }
 }
 template <int DT, int OP>

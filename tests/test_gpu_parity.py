@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 from oracle import closed_form, ring as oring, tree as otree
-from ring_allreduce_reduction_gb300.workloads import ELEM_SIZE, make_inputs
+from ring_allreduce_reduction_gb300.workloads import ELEM_SIZE, STORAGE, make_inputs
 from tests.gpu_harness import Buffers, run
 
 pytestmark = pytest.mark.gpu
@@ -278,5 +278,56 @@ def test_abort(v):
             v.vrcclAllReduce(b.send_ptrs(), b.recv_ptrs(), b.count, "float32", "sum", "ring", "simple", comm)
         torch.cuda.synchronize()
         assert v.RESULTS[v.vrcclCommGetAsyncError(comm)] == "vrcclAborted"
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+def _hostile_2byte(n, count, dtype, seed):
+    """Bit patterns of the type drawn over every exponent (NaN and infinity
+    excluded), a quarter of them subnormal, with zeros of both signs and
+    values next to the largest finite one; summing them rounds at every
+    exponent distance, overflows to infinity and meets subnormals."""
+    g = np.random.default_rng(seed)
+    if dtype == "bfloat16":
+        exp_bits, man_bits, max_finite = 8, 7, 0x7F7F
+    else:
+        exp_bits, man_bits, max_finite = 5, 10, 0x7BFF
+    emax = (1 << exp_bits) - 1
+    sign = g.integers(0, 2, (n, count), dtype=np.uint16) << 15
+    exp = g.integers(0, emax, (n, count), dtype=np.uint16)          # emax excluded: no inf/NaN
+    exp = np.where(g.random((n, count)) < 0.25, 0, exp).astype(np.uint16)  # subnormals and zeros
+    man = g.integers(0, 1 << man_bits, (n, count), dtype=np.uint16)
+    bits = (sign | (exp << man_bits) | man).astype(np.uint16)
+    pick = g.random((n, count))
+    bits = np.where(pick < 0.03, (sign | max_finite).astype(np.uint16), bits)
+    bits = np.where((pick >= 0.03) & (pick < 0.05), sign, bits)  # +0 / -0
+    return np.ascontiguousarray(bits.astype(np.uint16)).view(STORAGE[dtype])
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+@pytest.mark.parametrize("op", ["sum", "avg"])
+def test_two_byte_sums_on_hostile_values(v, dtype, op):
+    """The packed 2-byte add must give the oracle's bits (binary32 add, then
+    round to nearest even) at every exponent distance, on subnormals, signed
+    zeros and overflow, for every schedule that reduces."""
+    n, count = 8, 20000
+    x = _hostile_2byte(n, count, dtype, seed={"bfloat16": 10, "float16": 20}[dtype] + len(op))
+    comm = v.vrcclCommInit(n, 4)
+    try:
+        v.vrcclCommSetSchedule(comm, 3, 512)
+        for algo, proto in (("ring", "simple"), ("ring", "ll"), ("ring", "ll128"), ("tree", "simple"),
+                            ("tree", "ll"), ("oneshot", "simple")):
+            y, sched, b = run(v, comm, x, dtype, op, algo, proto)
+            ref = (otree.tree_allreduce(x, op, dtype, sched["nchannels"]) if sched["algo"] == "tree" else
+                   oring.ring_allreduce(x, op, dtype, sched["nchannels"], sched["chunk_elems"]))
+            # bits must match, except that any NaN equals any NaN (the tree can add
+            # +inf and -inf partial sums; NaN payloads are not part of the result)
+            exp_mask, man_mask = (0x7F80, 0x007F) if dtype == "bfloat16" else (0x7C00, 0x03FF)
+            yu, ru = y.view(np.uint16), ref.view(np.uint16)
+            nan_y = ((yu & exp_mask) == exp_mask) & ((yu & man_mask) != 0)
+            nan_r = ((ru & exp_mask) == exp_mask) & ((ru & man_mask) != 0)
+            bad = np.nonzero((yu != ru) & ~(nan_y & nan_r))
+            assert bad[0].size == 0, (algo, proto, bad[0].size, y.view(np.uint16)[bad][:4], ref.view(np.uint16)[bad][:4])
+            assert b.canaries_intact()
     finally:
         v.vrcclCommDestroy(comm)
