@@ -759,21 +759,63 @@ static bool isLive(vrcclComm* c) {
 // in NCCL's model), each task takes the channel count a call of its own
 // size would get, and tasks fill channel ranges round-robin. Every other
 // call runs alone.
-static vrcclResult_t launchRun(vrcclComm_t comm, const std::vector<Call>& calls, const std::vector<int>& run) {
+// A run with its launch shape and each task's channel count. A task whose
+// part on a channel is shorter than one ring loop (n chunks) pays the loop's
+// 2n-1 dependent steps with chunks too small to hide a hop's latency, so a
+// grouped task takes just enough channels to give each a full loop, at most
+// the launch's: the group's many tasks then run side by side on different
+// channels (measured on the 224-tensor bucket: 8.96 ms with each task on the
+// channels a call of its size would use, 13.2 ms with every task on all 19).
+struct PlannedRun {
+  Shape s;
+  std::vector<int> idx;
+  std::vector<int> nch;
+};
+
+static vrcclResult_t planRun(vrcclComm_t comm, const std::vector<Call>& calls, const std::vector<int>& run,
+                             PlannedRun* out) {
   const int n = comm->nranks;
   const Call& k0 = calls[run[0]];
   const size_t E = kElemSize[k0.dtype];
   size_t total = 0;
   for (int i : run) total += calls[i].count * E;
-  Shape s;
-  vrcclResult_t res = chooseShape(comm, kAllReduce, vrcclAlgoRing, k0.proto, total, k0.dtype, k0.op, E, true, &s);
+  vrcclResult_t res = chooseShape(comm, kAllReduce, vrcclAlgoRing, k0.proto, total, k0.dtype, k0.op, E, true,
+                                  &out->s);
   if (res != vrcclSuccess) return res;
-  const int sliceElems = (int)(s.sliceBytes / E);
+  out->idx = run;
+  out->nch.clear();
+  const size_t loopBytes = size_t(n) * out->s.chunkBytes;
+  for (int i : run) {
+    const size_t b = calls[i].count * E;
+    int nch = comm->forceChannels ? comm->forceChannels
+            : comm->envChannels   ? comm->envChannels
+                                  : (int)std::min<size_t>((b + loopBytes - 1) / loopBytes, (size_t)out->s.C);
+    out->nch.push_back(std::max(1, std::min(nch, out->s.C)));
+  }
+  return vrcclSuccess;
+}
+
+static bool sameLaunch(const Shape& a, const Shape& b) {
+  return a.fn == b.fn && a.C == b.C && a.threads == b.threads && a.stages == b.stages && a.smem == b.smem &&
+         a.sliceBytes == b.sliceBytes && a.chunkBytes == b.chunkBytes;
+}
+
+// Enqueues planned runs. Consecutive runs with the same launch shape share
+// launches (one plan holds a group's collectives, "NCCL architecture ...",
+// §9.6); a launch takes tasks until its parameter block is full. Within a
+// launch, each task (largest first) takes the window of channels whose most
+// loaded channel carries the fewest bytes so far.
+static vrcclResult_t launchRuns(vrcclComm_t comm, const std::vector<Call>& calls, const std::vector<PlannedRun>& runs) {
+  const int n = comm->nranks;
   const int maxTasks = std::min(kMaxGroupTasks, kGroupPtrs / n);
+  vrcclResult_t res = vrcclSuccess;
   GroupArgs* g = new GroupArgs;
-  size_t i0 = 0;
-  int cursor = 0;
-  while (i0 < run.size() && res == vrcclSuccess) {
+  size_t r = 0, t0 = 0;  // next run, next task within it
+  while (r < runs.size() && res == vrcclSuccess) {
+    const Shape& s = runs[r].s;
+    const Call& k0 = calls[runs[r].idx[0]];
+    const size_t E = kElemSize[k0.dtype];
+    const int sliceElems = (int)(s.sliceBytes / E);
     memset(static_cast<void*>(g), 0, sizeof(*g));
     g->comm = comm->dc;
     g->nranks = n;
@@ -783,29 +825,40 @@ static vrcclResult_t launchRun(vrcclComm_t comm, const std::vector<Call>& calls,
     g->stages = s.stages;
     g->prefetch = s.P == kSimple ? comm->envPrefetch : 0;
     g->scale = 1.0f / (float)n;
+    std::vector<double> load(s.C, 0.0);
     unsigned long long steps = 0;
     size_t bytes = 0;
     int t = 0;
-    for (; t < maxTasks && i0 + t < run.size(); ++t) {
-      const Call& k = calls[run[i0 + t]];
-      const size_t b = k.count * E;
-      const Choice own = comm->tuner.choose(n, b, comm->maxChannels, kRing, s.P);
-      int nch = comm->forceChannels ? comm->forceChannels
-              : comm->envChannels   ? comm->envChannels
-              : own.channels > 0    ? own.channels
-                                    : defaultChannels(s.P, b, n, comm->maxChannels);
-      nch = std::max(1, std::min(nch, s.C));
+    while (t < maxTasks && r < runs.size() && sameLaunch(runs[r].s, s)) {
+      const int ci = runs[r].idx[t0];
+      const Call& k = calls[ci];
+      const int nch = runs[r].nch[t0];
+      int best = 0;
+      double bestLoad = -1.0;
+      for (int st = 0; st < s.C; ++st) {
+        double m = 0.0;
+        for (int j = 0; j < nch; ++j) m = std::max(m, load[(st + j) % s.C]);
+        if (bestLoad < 0.0 || m < bestLoad) {
+          bestLoad = m;
+          best = st;
+        }
+      }
+      for (int j = 0; j < nch; ++j) load[(best + j) % s.C] += double(k.count * E) / nch;
       g->task[t].count = k.count;
-      g->task[t].chLo = cursor;
+      g->task[t].chLo = best;
       g->task[t].nch = nch;
-      cursor = (cursor + nch) % s.C;
-      for (int r = 0; r < n; ++r) {
-        g->send[t * n + r] = k.send[r];
-        g->recv[t * n + r] = k.recv[r];
+      for (int q = 0; q < n; ++q) {
+        g->send[t * n + q] = k.send[q];
+        g->recv[t * n + q] = k.recv[q];
       }
       steps += stepBound(n, k.count, nch, sliceElems);
-      bytes += b;
-      comm->groupSched[run[i0 + t]] = {kRing, s.P, nch, s.chunkBytes / E, comm->groupLaunches};
+      bytes += k.count * E;
+      comm->groupSched[ci] = {kRing, s.P, nch, s.chunkBytes / E, comm->groupLaunches};
+      ++t;
+      if (++t0 == runs[r].idx.size()) {
+        ++r;
+        t0 = 0;
+      }
     }
     g->ntasks = t;
     res = llReserve(comm, s.P, steps, k0.stream);
@@ -815,7 +868,6 @@ static vrcclResult_t launchRun(vrcclComm_t comm, const std::vector<Call>& calls,
       recordLast(comm, kRing, s, E, s.per * s.C);
       debugLine(comm, "AllReduce(group)", bytes, "Ring", s, s.per * s.C);
     }
-    i0 += t;
   }
   delete g;
   return res;
@@ -846,6 +898,7 @@ static vrcclResult_t runGroup(vrcclComm_t comm) {
     }
     it->second.push_back(i);
   }
+  std::vector<PlannedRun> planned;
   for (auto& b : buckets) {
     std::vector<int>& v = b.second;
     std::stable_sort(v.begin(), v.end(), [&](int a, int c) { return calls[a].count > calls[c].count; });
@@ -853,11 +906,12 @@ static vrcclResult_t runGroup(vrcclComm_t comm) {
     while (i < v.size() && res == vrcclSuccess) {
       size_t j = i + 1;
       while (j < v.size() && calls[v[i]].count < 4 * calls[v[j]].count) ++j;
-      std::vector<int> run(v.begin() + i, v.begin() + j);
-      res = launchRun(comm, calls, run);
+      planned.emplace_back();
+      res = planRun(comm, calls, std::vector<int>(v.begin() + i, v.begin() + j), &planned.back());
       i = j;
     }
   }
+  if (res == vrcclSuccess) res = launchRuns(comm, calls, planned);
   for (size_t a = 0; a < alone.size() && res == vrcclSuccess; ++a) {
     const Call& k = calls[alone[a]];
     res = runCall(comm, k);

@@ -124,9 +124,15 @@ def test_mixed_group_matches_oracle_and_aggregation_rule(v):
         tasks = [((spec[i][0], spec[i][1], spec[i][4]), spec[i][2]) for i in ringable]
         runs = [[ringable[j] for j in run] for run in ogroup.aggregate(tasks)]
         launch_of = {i: scheds[i]["launch"] for i in ringable}
-        for run in runs:
+        for run in runs:  # a run is scheduled as a whole: one launch
             assert len({launch_of[i] for i in run}) == 1, run
-        assert len({launch_of[run[0]] for run in runs}) == len(runs)
+        # runs with the same launch shape may share a launch; calls of
+        # different runs never share one unless their whole runs do
+        for a in runs:
+            for b in runs:
+                if launch_of[a[0]] == launch_of[b[0]]:
+                    assert scheds[a[0]]["proto"] == scheds[b[0]]["proto"]
+        assert len(set(launch_of.values())) <= len(runs)
         assert [2, 4] in runs and [0, 1] in runs
     finally:
         v.vrcclCommDestroy(comm)
@@ -163,8 +169,8 @@ def test_gradient_bucket_as_224_grouped_calls(v):
             ref = oring.ring_allreduce(x[:, a:b], "avg", "bfloat16", s["nchannels"], s["chunk_elems"])
             assert _same(y[:, a:b], ref), (t, s)
         tasks = [("bf16avg", int(sz)) for sz in sizes]
-        assert len(launches) >= len(ogroup.aggregate(tasks))
-        assert len(launches) < 40, "224 calls should need only a few launches"
+        assert len(launches) <= len(ogroup.aggregate(tasks)) + 224 * 8 // 1536 + 1
+        assert len(launches) < 12, "224 calls should need only a few launches"
     finally:
         v.vrcclCommDestroy(comm)
 
