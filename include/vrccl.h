@@ -141,8 +141,9 @@ typedef enum {
  *         vrcclCudaError (no device, allocation failed; nothing is leaked).
  * Environment, read once here: VRCCL_TIMEOUT_MS (device wait limit,
  * default 2000), VRCCL_DEBUG=INFO (prints each call's decision line),
- * VRCCL_PROTO / VRCCL_ALGO (simple|ll|ll128 / ring|tree: what "auto"
- * resolves to), VRCCL_NCHANNELS (channel count "auto" uses),
+ * VRCCL_ALGO / VRCCL_PROTO (NCCL_ALGO / NCCL_PROTO's list syntax, see
+ * vrcclParseList: what "auto" may choose; an unknown name makes this call
+ * return vrcclInvalidArgument), VRCCL_NCHANNELS (channel count "auto" uses),
  * VRCCL_SLICE_BYTES (largest Simple FIFO slot to use, bytes; default and
  * most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent, at
  * most 16; default 16 for 2-byte types, 8 for 4-byte ones), VRCCL_PREFETCH (input slices a Simple agent pulls into L2
@@ -272,6 +273,55 @@ vrcclResult_t vrcclGroupEnd(void);
  */
 vrcclResult_t vrcclCommGetGroupSchedule(vrcclComm_t comm, int index, int* algo, int* proto, int* nchannels,
                                         size_t* chunkElems, int* launch);
+
+/*
+ * vrcclParseList -- the list syntax of VRCCL_ALGO / VRCCL_PROTO, which is
+ * NCCL_ALGO / NCCL_PROTO's (parseList, [Architecture §8.5]): elements are
+ * comma separated; a leading '^' excludes the listed names instead; a
+ * "function:" prefix restricts a list to one collective; ';' separates
+ * lists, the first of which may have no prefix (it applies to every
+ * collective). Names are case-insensitive and are NCCL's: functions
+ * Broadcast, Reduce, AllGather, ReduceScatter, AllReduce; algorithms Tree,
+ * Ring, CollNetDirect, CollNetChain, NVLS, NVLSTree, PAT; protocols LL,
+ * LL128, Simple. Of those this library has Ring and Tree (AllReduce; the
+ * others are ring-only) and all three protocols; "auto" chooses among the
+ * allowed ones, and a call left with none returns vrcclInvalidUsage.
+ *   spec   the string (NULL or empty: everything allowed).
+ *   kind   0 = algorithms, 1 = protocols.
+ *   masks  out: 5 masks, one per function in the order above; bit i is the
+ *          i-th name of the kind in the order above.
+ * Errors: vrcclInvalidArgument for an unknown name (then vrcclCommInit
+ * refuses the same string in the environment).
+ */
+vrcclResult_t vrcclParseList(const char* spec, int kind, unsigned* masks);
+
+/*
+ * vrcclModelPredict -- the pages' analytic model of an AllReduce's time,
+ * T = latency * numPipeOps(ring) + bytes / (1000 * algorithm bandwidth) us
+ * (ncclTopoTuneModel / ncclTopoGetAlgoTime, [Architecture §8.1-§8.3]),
+ * with the constants the pages print. It serves to set the measured tuning
+ * table beside the pages' model; the library never schedules by it.
+ *   graph      ranks, nodes, channels, per-channel link bandwidth (GB/s)
+ *              inside a node and across nodes, extra latency per inter-node
+ *              step (us), intra-node hardware (0 NVLink, 1 PCI), GPU
+ *              architecture (0 Volta, 1 Ampere, 2 Hopper, 3 Blackwell).
+ *   algo       ring or tree; proto: simple, ll or ll128.
+ *   bytes      message size; numPipeOps: operations aggregated with it (>= 1).
+ *   latUs, algBwGBs, timeUs  out (each may be NULL).
+ * Errors: vrcclInvalidArgument for an inconsistent graph or a bad enum.
+ */
+typedef struct {
+  int nranks;
+  int nnodes;
+  int nchannels;
+  float bwIntra;
+  float bwInter;
+  float latencyInter;
+  int hwIntra;
+  int arch;
+} vrcclModelGraph_t;
+vrcclResult_t vrcclModelPredict(const vrcclModelGraph_t* graph, vrcclAlgo_t algo, vrcclProto_t proto, size_t bytes,
+                                int numPipeOps, float* latUs, float* algBwGBs, float* timeUs);
 
 /*
  * vrcclCommSetSchedule -- pin the channel count and chunk size used by

@@ -29,12 +29,18 @@ static int log2Bucket(size_t bytes) {
   return b;
 }
 
-Choice Tuner::choose(int nranks, size_t bytes, int maxChannels, int algo, int proto) const {
-  Choice c{algo >= 0 ? algo : kRing,
-           proto >= 0 ? proto : (bytes <= 65536 ? kLL : bytes <= (size_t(2) << 20) ? kLL128 : kSimple), 0, 0, 0};
+Choice Tuner::choose(int nranks, size_t bytes, int maxChannels, unsigned algoMask, unsigned protoMask) const {
+  // the size rule's preference order, first allowed protocol wins
+  static const int kSmall[3] = {kLL, kLL128, kSimple}, kMid[3] = {kLL128, kSimple, kLL},
+                   kLarge[3] = {kSimple, kLL128, kLL};
+  const int* pref = bytes <= 65536 ? kSmall : bytes <= (size_t(2) << 20) ? kMid : kLarge;
+  int proto = pref[0];
+  for (int i = 2; i >= 0; --i)
+    if (protoMask & (1u << pref[i])) proto = pref[i];
+  Choice c{(algoMask & (1u << kRing)) ? kRing : kTree, proto, 0, 0, 0};
   auto eligible = [&](const Entry& e) {
-    return e.nranks == nranks && e.channels <= maxChannels && (algo < 0 || e.algo == algo) &&
-           (proto < 0 || e.proto == proto);
+    return e.nranks == nranks && e.channels <= maxChannels && (algoMask & (1u << e.algo)) &&
+           (protoMask & (1u << e.proto));
   };
   const int want = log2Bucket(bytes);
   int bestDist = 1 << 30;

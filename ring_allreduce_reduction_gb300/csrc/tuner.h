@@ -7,8 +7,9 @@
 // measured on this GPU for this communicator's rank count: per (algo,
 // proto, channels, slice size) and per power-of-two message size, and the
 // choice is the measured minimum at the nearest size. Without a table the
-// rule below stands in: LL up to 64 KiB, LL128 up to 2 MiB, Simple beyond,
-// and NCCL's channel shrink (§6.4 of the same page).
+// rule below stands in: LL up to 64 KiB, LL128 up to 2 MiB, Simple beyond
+// (the nearest allowed protocol in that order of preference), the ring if
+// allowed, and NCCL's channel shrink (§6.4 of the same page).
 #pragma once
 
 #include <cstddef>
@@ -38,8 +39,10 @@ class Tuner {
     size_t sliceBytes;
     double us;
   };
-  // algo / proto: -1 = free, else only entries with that value are eligible.
-  Choice choose(int nranks, size_t bytes, int maxChannels, int algo = -1, int proto = -1) const;
+  // Only entries whose algorithm is in algoMask (bit kRing, bit kTree) and
+  // whose protocol is in protoMask (bits kSimple, kLL, kLL128) are eligible;
+  // a mask with one bit forces that choice. Masks must not be empty.
+  Choice choose(int nranks, size_t bytes, int maxChannels, unsigned algoMask = 3u, unsigned protoMask = 7u) const;
   // Reads VRCCL_TUNE_FILE if set, else the table shipped next to the
   // library (tuning/gb300_n<nranks>.txt) if there is one. Format: one entry
   // per line, "nranks algo proto channels log2bytes sliceBytes

@@ -17,6 +17,8 @@
 #include <utility>
 #include <vector>
 
+#include "model.h"
+#include "parse.h"
 #include "tuner.h"
 #include "vrccl_internal.h"
 
@@ -95,7 +97,11 @@ struct vrcclComm {
   // schedule
   int forceChannels;
   size_t forceChunkBytes;
-  int envProto, envAlgo, envChannels;
+  // VRCCL_ALGO / VRCCL_PROTO per collective (index CollId): algorithms
+  // (bit kRing, bit kTree) and protocols (bits kSimple, kLL, kLL128) "auto"
+  // may choose.
+  unsigned envAlgoMask[3], envProtoMask[3];
+  int envChannels;
   size_t envSliceBytes;
   int envWarps, envPrefetch;
   bool debug;
@@ -126,22 +132,19 @@ static int envInt(const char* name, int dflt) {
   return atoi(v);
 }
 
-static int parseProto(const char* v) {
-  if (!v) return -1;
-  std::string s(v);
-  for (auto& ch : s) ch = (char)tolower(ch);
-  if (s == "simple") return kSimple;
-  if (s == "ll") return kLL;
-  if (s == "ll128") return kLL128;
-  return -1;
-}
-static int parseAlgo(const char* v) {
-  if (!v) return -1;
-  std::string s(v);
-  for (auto& ch : s) ch = (char)tolower(ch);
-  if (s == "ring") return kRing;
-  if (s == "tree") return kTree;
-  return -1;
+// VRCCL_ALGO / VRCCL_PROTO (NCCL's parseList syntax) -> per-collective
+// masks in this library's ids; false for a string with an unknown name.
+static bool envMasks(unsigned algoMask[3], unsigned protoMask[3]) {
+  unsigned a[kNumParseFuncs], p[kNumParseFuncs];
+  if (parseList(getenv("VRCCL_ALGO"), kParseAlgo, a) != 0) return false;
+  if (parseList(getenv("VRCCL_PROTO"), kParseProto, p) != 0) return false;
+  static const int kFn[3] = {kFnAllReduce, kFnReduceScatter, kFnAllGather};  // by CollId
+  for (int c = 0; c < 3; ++c) {
+    const unsigned am = a[kFn[c]], pm = p[kFn[c]];
+    algoMask[c] = ((am >> 1) & 1u) << kRing | (am & 1u) << kTree;          // NCCL: Tree bit 0, Ring bit 1
+    protoMask[c] = (pm & 1u) << kLL | ((pm >> 1) & 1u) << kLL128 | ((pm >> 2) & 1u) << kSimple;
+  }
+  return true;
 }
 
 static const char* kAlgoName[4] = {"Ring", "Tree", "Auto", "OneShot"};
@@ -236,8 +239,10 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
   c->dc.timeoutNs = (unsigned long long)tmo * 1000000ull;
   const char* dbg = getenv("VRCCL_DEBUG");
   c->debug = dbg && (strcasecmp(dbg, "INFO") == 0 || strcasecmp(dbg, "TRACE") == 0);
-  c->envProto = parseProto(getenv("VRCCL_PROTO"));
-  c->envAlgo = parseAlgo(getenv("VRCCL_ALGO"));
+  if (!envMasks(c->envAlgoMask, c->envProtoMask)) {
+    freeComm(c);
+    return vrcclInvalidArgument;  // "Unrecognized element token"
+  }
   c->envChannels = std::min(envInt("VRCCL_NCHANNELS", 0), nchannels);
   c->envSliceBytes = (size_t)std::max(0, envInt("VRCCL_SLICE_BYTES", 0)) / 16 * 16;
   c->envWarps = std::max(0, envInt("VRCCL_SIMPLE_WARPS", 0));
@@ -495,14 +500,21 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
   const int n = comm->nranks;
   const bool userAlgo = coll == kAllReduce && algo != vrcclAlgoAuto && !grouped;
   const bool userProto = proto != vrcclProtoAuto;
-  const int fixA = (coll != kAllReduce || grouped || algo == vrcclAlgoOneShot) ? kRing
-                 : userAlgo ? algo : comm->envAlgo;
-  const int fixP = algo == vrcclAlgoOneShot ? kSimple : userProto ? proto : comm->envProto;
-  Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, n == 1 ? kRing : fixA, fixP);
+  // What "auto" may choose: the environment's lists, narrowed by the call
+  // (an explicit algorithm or protocol is the only choice) and by what the
+  // collective has (the phases, a group's runs and the one-shot's order
+  // are the ring's). An empty choice is NCCL's "no algorithm/protocol
+  // available".
+  unsigned algoMask = comm->envAlgoMask[coll], protoMask = comm->envProtoMask[coll];
+  if (userAlgo && algo != vrcclAlgoOneShot) algoMask = 1u << algo;
+  if (coll != kAllReduce || grouped || algo == vrcclAlgoOneShot || n == 1) algoMask &= 1u << kRing;
+  if (algo == vrcclAlgoOneShot || n == 1) algoMask = 1u << kRing;  // a single rank is a local copy
+  if (userProto) protoMask = 1u << proto;
+  if (algo == vrcclAlgoOneShot) protoMask = 1u << kSimple;
+  if (!algoMask || !protoMask) return vrcclInvalidUsage;
+  Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, algoMask, protoMask);
   if (tuned) *tuned = ch;
-  int A = fixA >= 0 ? fixA : ch.algo;
-  int P = fixP >= 0 ? fixP : ch.proto;
-  if (n == 1) A = kRing;  // a single rank is a local copy (ncclLaunchOneRank)
+  const int A = ch.algo, P = ch.proto;
   int C = comm->forceChannels ? comm->forceChannels
         : comm->envChannels   ? comm->envChannels
         : (ch.channels > 0 ? std::min(ch.channels, comm->maxChannels)
@@ -885,7 +897,8 @@ static vrcclResult_t runGroup(vrcclComm_t comm) {
   for (int i = 0; i < (int)calls.size(); ++i) {
     const Call& k = calls[i];
     const bool ringable = k.coll == kAllReduce && comm->nranks > 1 && k.count > 0 &&
-                          (k.algo == vrcclAlgoRing || (k.algo == vrcclAlgoAuto && comm->envAlgo != kTree));
+                          (k.algo == vrcclAlgoRing ||
+                           (k.algo == vrcclAlgoAuto && (comm->envAlgoMask[kAllReduce] & (1u << kRing))));
     if (!ringable) {
       alone.push_back(i);
       continue;
@@ -1025,3 +1038,28 @@ extern "C" vrcclResult_t vrcclCommLoadTuning(vrcclComm_t comm, const char* path,
   if (loaded) *loaded = k;
   return vrcclSuccess;
 }
+
+extern "C" vrcclResult_t vrcclParseList(const char* spec, int kind, unsigned* masks) {
+  if (!masks || (kind != 0 && kind != 1)) return vrcclInvalidArgument;
+  return parseList(spec, kind == 0 ? kParseAlgo : kParseProto, masks) == 0 ? vrcclSuccess : vrcclInvalidArgument;
+}
+
+extern "C" vrcclResult_t vrcclModelPredict(const vrcclModelGraph_t* graph, vrcclAlgo_t algo, vrcclProto_t proto,
+                                           size_t bytes, int numPipeOps, float* latUs, float* algBwGBs,
+                                           float* timeUs) {
+  if (!graph || (algo != vrcclAlgoRing && algo != vrcclAlgoTree) || (unsigned)proto >= (unsigned)vrcclProtoAuto)
+    return vrcclInvalidArgument;
+  const vrcclModelGraph_t& g = *graph;
+  if (g.nranks < 2 || g.nnodes < 1 || g.nranks % g.nnodes || g.nchannels < 1 || g.bwIntra <= 0 ||
+      (g.nnodes > 2 && g.bwInter <= 0) || g.hwIntra < 0 || g.hwIntra > 1 || g.arch < 0 || g.arch > 3 ||
+      numPipeOps < 1)
+    return vrcclInvalidArgument;
+  ModelGraph m{g.nranks, g.nnodes, g.nchannels, g.bwIntra, g.bwInter, g.latencyInter, g.hwIntra, g.arch};
+  double lat[2][3], bw[2][3];
+  modelTable(m, lat, bw);
+  if (latUs) *latUs = (float)lat[algo][proto];
+  if (algBwGBs) *algBwGBs = (float)bw[algo][proto];
+  if (timeUs) *timeUs = (float)modelTime(m, algo, proto, bytes, numPipeOps);
+  return vrcclSuccess;
+}
+

@@ -14,6 +14,9 @@ Usage (on the GPU):
 
 Table format (one entry per line, '#' comments):
     nranks algo proto channels log2bytes sliceBytes microseconds
+
+    python -m ring_allreduce_reduction_gb300.tune --compare table.txt
+prints a table beside the pages' analytic model (no GPU needed).
 """
 from __future__ import annotations
 
@@ -106,8 +109,63 @@ def write_table(records: list[dict], path: str, header: str = "") -> None:
                     f"{r['us']:.3f}\n")
 
 
+def read_table(path: str) -> list[dict]:
+    alg = {0: "ring", 1: "tree"}
+    pro = {0: "simple", 1: "ll", 2: "ll128"}
+    recs = []
+    for ln in open(path):
+        ln = ln.split("#", 1)[0].split()
+        if len(ln) == 7:
+            n, a, p, c, lg, sl, us = ln
+            recs.append({"nranks": int(n), "algo": alg[int(a)], "proto": pro[int(p)], "channels": int(c),
+                         "bytes": 1 << int(lg), "slice_bytes": int(sl), "us": float(us)})
+    return recs
+
+
+def compare(recs: list[dict], arch: str = "blackwell", hw: str = "nvlink") -> list[dict]:
+    """The measured table beside the pages' model (vrcclModelPredict), as
+    the pages' log reader sets NCCL's printed tuning table against measured
+    times. The model's one free input is the per-channel link bandwidth:
+    here the ring/Simple bus bandwidth per channel at the table's largest
+    size. Returns one row per size: the measured best, the model's best and
+    the ratio measured / model for the measured best's (algo, proto)."""
+    from ring_allreduce_reduction_gb300 import vrccl as v
+    n = recs[0]["nranks"]
+    big = max(r["bytes"] for r in recs)
+    simple = [r for r in recs if r["bytes"] == big and r["algo"] == "ring" and r["proto"] == "simple"]
+    best_big = min(simple, key=lambda r: r["us"])
+    C = best_big["channels"]
+    busbw = big / (best_big["us"] * 1e-6) * 2 * (n - 1) / n / 1e9
+    bw_link = busbw / C
+    rows = []
+    for size in sorted({r["bytes"] for r in recs}):
+        here = [r for r in recs if r["bytes"] == size]
+        meas = min(here, key=lambda r: r["us"])
+        model = {}
+        for a in ("ring", "tree"):
+            for p in ("simple", "ll", "ll128"):
+                model[(a, p)] = v.vrcclModelPredict(n, 1, C, bw_link, a, p, size, arch=arch, hw_intra=hw)["time_us"]
+        mbest = min(model, key=model.get)
+        rows.append({"bytes": size, "measured": (meas["algo"], meas["proto"], meas["channels"], meas["us"]),
+                     "model": (mbest[0], mbest[1], model[mbest]),
+                     "ratio": meas["us"] / model[(meas["algo"], meas["proto"])]})
+    return rows, {"nranks": n, "channels": C, "bw_link_gbs": bw_link, "arch": arch, "hw": hw}
+
+
+def print_compare(rows, graph) -> None:
+    print(f"# measured table vs the pages' model: {graph['nranks']} ranks, {graph['channels']} channels x "
+          f"{graph['bw_link_gbs']:.1f} GB/s (fitted), {graph['hw']} latencies, {graph['arch']} constants")
+    print(f"{'bytes':>12} | {'measured best':>28} | {'model best':>24} | measured/model")
+    for r in rows:
+        a, p, c, us = r["measured"]
+        ma, mp, mus = r["model"]
+        print(f"{r['bytes']:>12} | {a + '/' + p + ' C=' + str(c):>17} {us:9.1f} us | {ma + '/' + mp:>13} "
+              f"{mus:8.1f} us | {r['ratio']:6.2f}")
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
+    ap.add_argument("--compare", default="", help="print a measured table beside the pages' model and exit")
     ap.add_argument("--nranks", type=int, default=8)
     ap.add_argument("--dtype", default="bfloat16", choices=list(ELEM))
     ap.add_argument("--op", default="sum")
@@ -121,6 +179,10 @@ def main() -> int:
     ap.add_argument("--out", default="")
     ap.add_argument("--json", default="")
     args = ap.parse_args()
+    if args.compare:
+        rows, graph = compare(read_table(args.compare))
+        print_compare(rows, graph)
+        return 0
     sizes, b = [], args.min_bytes
     while b <= args.max_bytes:
         sizes.append(b)

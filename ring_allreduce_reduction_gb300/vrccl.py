@@ -51,6 +51,10 @@ _sig = {
     "vrcclGroupEnd": [],
     "vrcclCommGetGroupSchedule": [ctypes.c_void_p, ctypes.c_int, _c_int_p, _c_int_p, _c_int_p,
                                   ctypes.POINTER(ctypes.c_size_t), _c_int_p],
+    "vrcclParseList": [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint)],
+    "vrcclModelPredict": [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_size_t, ctypes.c_int,
+                          ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
+                          ctypes.POINTER(ctypes.c_float)],
     "vrcclCommSetSchedule": [ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t],
     "vrcclCommGetLastSchedule": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p, ctypes.POINTER(ctypes.c_size_t)],
     "vrcclCommGetAsyncError": [ctypes.c_void_p, _c_int_p],
@@ -168,6 +172,37 @@ def vrcclCommGetGroupSchedule(comm, index: int) -> dict:
                                           ctypes.byref(k), ctypes.byref(l)), "vrcclCommGetGroupSchedule")
     return {"algo": ALGO_NAMES[a.value], "proto": PROTO_NAMES[p.value], "nchannels": c.value,
             "chunk_elems": k.value, "launch": l.value}
+
+
+PARSE_FUNCS = ["broadcast", "reduce", "allgather", "reducescatter", "allreduce"]
+PARSE_NAMES = {0: ["tree", "ring", "collnetdirect", "collnetchain", "nvls", "nvlstree", "pat"],
+               1: ["ll", "ll128", "simple"]}
+
+
+class _ModelGraph(ctypes.Structure):
+    _fields_ = [("nranks", ctypes.c_int), ("nnodes", ctypes.c_int), ("nchannels", ctypes.c_int),
+                ("bwIntra", ctypes.c_float), ("bwInter", ctypes.c_float), ("latencyInter", ctypes.c_float),
+                ("hwIntra", ctypes.c_int), ("arch", ctypes.c_int)]
+
+
+def vrcclParseList(spec, kind: str) -> dict:
+    """{function: sorted list of allowed names}; kind "algo" or "proto"."""
+    k = {"algo": 0, "proto": 1}[kind]
+    masks = (ctypes.c_uint * 5)()
+    _check(_lib.vrcclParseList(None if spec is None else spec.encode(), k, masks), "vrcclParseList")
+    return {f: [nm for i, nm in enumerate(PARSE_NAMES[k]) if masks[j] >> i & 1] for j, f in enumerate(PARSE_FUNCS)}
+
+
+def vrcclModelPredict(nranks: int, nnodes: int, nchannels: int, bw_intra: float, algo, proto, nbytes: int,
+                      num_pipe_ops: int = 1, bw_inter: float = 0.0, latency_inter: float = 0.0, hw_intra: str = "nvlink",
+                      arch: str = "hopper") -> dict:
+    g = _ModelGraph(nranks, nnodes, nchannels, bw_intra, bw_inter, latency_inter,
+                    {"nvlink": 0, "pci": 1}[hw_intra], {"volta": 0, "ampere": 1, "hopper": 2, "blackwell": 3}[arch])
+    lat, bw, t = ctypes.c_float(), ctypes.c_float(), ctypes.c_float()
+    _check(_lib.vrcclModelPredict(ctypes.byref(g), _enum(ALGOS, algo, "algo"), _enum(PROTOS, proto, "proto"), nbytes,
+                                  num_pipe_ops, ctypes.byref(lat), ctypes.byref(bw), ctypes.byref(t)),
+           "vrcclModelPredict")
+    return {"lat_us": lat.value, "algbw_gbs": bw.value, "time_us": t.value}
 
 
 def vrcclCommSetSchedule(comm, nchannels: int = 0, chunkBytes: int = 0) -> None:

@@ -67,3 +67,55 @@ def test_shipped_table_is_found_for_8_ranks(v):
         _check(x, y, sched)
     finally:
         v.vrcclCommDestroy(comm)
+
+
+def test_env_lists_steer_auto(v, monkeypatch):
+    """VRCCL_ALGO / VRCCL_PROTO in NCCL's list syntax, read when the
+    communicator is made: per-collective restrictions, exclusions, and
+    NCCL's "no algorithm available" when nothing is left."""
+    import torch
+    n = 8
+    x = torch.randn((n, 1 << 16), device="cuda:0")
+    y = torch.empty_like(x)
+    rs = torch.empty((n, (1 << 16) // n), device="cuda:0")
+
+    def ar(comm):
+        v.vrcclAllReduce([x[r] for r in range(n)], [y[r] for r in range(n)], 1 << 16, "float32", "sum", "auto",
+                         "auto", comm)
+        return v.vrcclCommGetLastSchedule(comm)
+
+    def red_scat(comm):
+        v.vrcclReduceScatter([x[r] for r in range(n)], [rs[r] for r in range(n)], (1 << 16) // n, "float32", "sum",
+                             "auto", comm)
+        return v.vrcclCommGetLastSchedule(comm)
+
+    monkeypatch.setenv("VRCCL_ALGO", "ring;allreduce:tree")
+    monkeypatch.setenv("VRCCL_PROTO", "^ll;allreduce:LL128")
+    comm = v.vrcclCommInit(n, 8)
+    try:
+        s = ar(comm)
+        assert (s["algo"], s["proto"]) == ("tree", "ll128")
+        s = red_scat(comm)
+        assert s["algo"] == "ring" and s["proto"] in ("simple", "ll128")
+        s = v.vrcclAllReduce([x[r] for r in range(n)], [y[r] for r in range(n)], 1 << 16, "float32", "sum", "ring",
+                             "simple", comm)  # an explicit choice overrides the lists
+        s = v.vrcclCommGetLastSchedule(comm)
+        assert (s["algo"], s["proto"]) == ("ring", "simple")
+        torch.cuda.synchronize()
+        assert v.vrcclCommGetAsyncError(comm) == 0
+    finally:
+        v.vrcclCommDestroy(comm)
+    monkeypatch.setenv("VRCCL_ALGO", "tree")  # the phases have only the ring
+    monkeypatch.delenv("VRCCL_PROTO")
+    comm = v.vrcclCommInit(n, 8)
+    try:
+        assert ar(comm)["algo"] == "tree"
+        with pytest.raises(v.VrcclError) as e:
+            red_scat(comm)
+        assert e.value.name == "vrcclInvalidUsage"
+    finally:
+        v.vrcclCommDestroy(comm)
+    monkeypatch.setenv("VRCCL_ALGO", "ring,torus")
+    with pytest.raises(v.VrcclError) as e:
+        v.vrcclCommInit(n, 8)
+    assert e.value.name == "vrcclInvalidArgument"
