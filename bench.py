@@ -383,6 +383,8 @@ def main() -> int:
     ap.add_argument("--algo", default="ring", choices=["ring", "tree", "oneshot"],
                     help="allreduce only: the schedule timed (the workload's is the ring)")
     ap.add_argument("--no-bound", action="store_true", help="skip timing the one-shot bound beside the ring")
+    ap.add_argument("--direct", action="store_true",
+                    help="ring AllReduce with the direct all-gather (through the recv buffers)")
     ap.add_argument("--bucket", default="", choices=["", "flat", "group", "separate"],
                     help="time the 224-tensor bf16 gradient bucket instead of the workload")
     ap.add_argument("--bytes-per-rank", type=int, default=0,
@@ -428,6 +430,9 @@ def main() -> int:
     recv = torch.empty((n, block) if coll == "reduce_scatter" else (n, count), dtype=send.dtype, device=send.device)
     sp, rp = [send[r] for r in range(n)], [recv[r] for r in range(n)]
     comm = v.vrcclCommInit(n, W["max_channels"])
+    if args.direct:
+        v.vrcclCommSetDirect(comm, True)
+        W["name"] += "_direct"
     stream = torch.cuda.current_stream()
 
     def step():
@@ -480,7 +485,7 @@ def main() -> int:
     mean_kern_s = statistics.mean(kern_ms) / 1e3
     peak, peak_kind = measured_peak()
     achieved = algo_bytes / mean_kern_s / 1e9
-    traffic = profiled_traffic(S) if coll == "allreduce" else None
+    traffic = profiled_traffic(S) if coll == "allreduce" and not args.direct and W["algo"] == "ring" else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",

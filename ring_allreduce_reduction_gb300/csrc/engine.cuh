@@ -27,8 +27,10 @@ enum SliceFlags : int {
   F_IN = 1,    // read this agent's input (pre-scaled) into the reduction
   F_OUT = 2,   // write the result to this agent's recv buffer
   F_POST = 4,  // apply the post-op (int32 avg)
-  F_RECV = 8,  // receive on every in-edge
-  F_SEND = 16  // send on every out-edge
+  F_RECV = 8,    // receive on every in-edge
+  F_SEND = 16,   // send on every out-edge
+  F_DRECV = 32,  // direct: the slice was written into this agent's recv buffer by its predecessor
+  F_DSEND = 64   // direct: write the result into the next rank's recv buffer
 };
 
 struct Agent {
@@ -38,6 +40,8 @@ struct Agent {
   unsigned long long rstep[2], sstep[2];
   int slices;     // FIFO steps done in this launch (fault injection clock)
   bool faulty;    // this agent is the injected fault
+  int dre, dse;   // direct edges (ring, Simple): in and out, -1 if none
+  unsigned long long drstep, dsstep;
 
   __device__ __forceinline__ void init(const DevComm& c, int proto_, int rank_, int ch_) {
     proto = proto_;
@@ -45,6 +49,8 @@ struct Agent {
     ch = ch_;
     nrecv = nsend = 0;
     slices = 0;
+    dre = dse = -1;
+    drstep = dsstep = 0;
     faulty = (c.faultRank == rank_ && c.faultChannel == ch_);
   }
   __device__ __forceinline__ void addRecv(const DevComm& c, int e) {
@@ -59,6 +65,14 @@ struct Agent {
     sstep[nsend] = ldRelaxed(&c.ctrl[proto][e].tail);  // posted by this agent last launch
     ++nsend;
   }
+  // The direct all-gather edges of a ring agent: recv from the previous
+  // rank's edge, send on its own (the counters continue across launches).
+  __device__ __forceinline__ void addDirect(const DevComm& c, int inEdge, int outEdge) {
+    dre = inEdge;
+    dse = outEdge;
+    drstep = ldRelaxed(&c.dctrl[inEdge].head);
+    dsstep = ldRelaxed(&c.dctrl[outEdge].tail);
+  }
   __device__ __forceinline__ bool faultNow(const DevComm& c) const { return faulty && slices >= c.faultAfter; }
   __device__ __forceinline__ char* slot(const DevComm& c, int e, unsigned long long step) const {
     return c.fifo[proto] + (size_t(e) * kSteps + size_t(step % kSteps)) * slotBufferBytes(proto);
@@ -69,6 +83,10 @@ struct Agent {
     if (flags & F_SEND)
       for (int i = 0; i < nsend; ++i) ++sstep[i];
     ++slices;
+  }
+  __device__ __forceinline__ void advanceDirect(int flags) {
+    if (flags & F_DRECV) ++drstep;
+    if (flags & F_DSEND) ++dsstep;
   }
   // LL / LL128 keep the sender's step only in registers during a launch;
   // store it so the next launch continues the flag sequence.

@@ -36,12 +36,12 @@ __device__ __forceinline__ void channelRange(unsigned long long count, int C, in
 // alignUp(ceil(rem/n), 16 bytes). A chunk moves as slices of at most
 // sliceElems elements, one FIFO step each.
 // One ring agent's slice sequence through its protocol.
-template <int PROTO, int DT, int OP, class Args, class It>
+template <int PROTO, int DT, int OP, bool DIRECT = false, class Args, class It>
 __device__ __forceinline__ void ringAgent(const Args& a, Agent& ag, It& it, const char* in, char* out) {
   using S = typename Ty<DT>::S;
   constexpr long long E = sizeof(S);
   if constexpr (PROTO == kSimple) {
-    simplePipeline<DT, OP, false>(a, ag, it, in, out);
+    simplePipeline<DT, OP, false, DIRECT>(a, ag, it, in, out);
   } else {
     SliceDesc d;
     while (it.next(d))
@@ -72,10 +72,19 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) ringKernel(const __gri
     ag.addRecv(c, ringEdge(ch, (r - 1 + n) % n, n));
     ag.addSend(c, ringEdge(ch, r, n));
   }
+  const bool direct = PROTO == kSimple && a.direct && a.coll == kAllReduce && n > 1;
+  if (direct) ag.addDirect(c, ringEdge(ch, (r - 1 + n) % n, n), ringEdge(ch, r, n));
   if (a.coll == kAllReduce || n == 1) {
     RingIter it;
-    it.init(n, r, (long long)lo, (long long)(hi - lo), a.chunkElems, 16 / E, a.sliceElems);
-    ringAgent<PROTO, DT, OP>(a, ag, it, in, out);
+    it.init(n, r, (long long)lo, (long long)(hi - lo), a.chunkElems, 16 / E, a.sliceElems, direct);
+    if constexpr (PROTO == kSimple) {
+      if (direct)
+        ringAgent<PROTO, DT, OP, true>(a, ag, it, in, out);
+      else
+        ringAgent<PROTO, DT, OP, false>(a, ag, it, in, out);
+    } else {
+      ringAgent<PROTO, DT, OP>(a, ag, it, in, out);
+    }
   } else {
     PhaseIter it;
     it.init(n, r, a.coll == kAllGather, (long long)lo, (long long)(hi - lo), (long long)a.count, a.chunkElems,

@@ -29,17 +29,25 @@ struct SliceDesc {
 // `slice` elements, one FIFO step each. With n == 1 the sequence is a copy.
 // Positions are element offsets from the start of the rank's buffers; the
 // channel's range starts at `lo`.
+//
+// direct (Simple): the directRecvCopyDirectSend form of the same primitives
+// for ranks that can address each other's buffers: the all-gather moves
+// through the recv buffers. The step that finishes chunk r writes it to
+// this rank's recv buffer and into the next rank's; an all-gather step
+// takes the chunk from this rank's recv buffer (where the predecessor wrote
+// it) and writes it into the next rank's; the last step only counts.
 struct RingIter {
   int n, r;
   long long lo, chCount, K, A, slice;
   long long off, rem, k, s, cHi;
   int p, flags;
-  bool started;
+  bool started, direct;
 
   __device__ __forceinline__ void init(int n_, int r_, long long lo_, long long chCount_, long long K_, long long A_,
-                                       long long slice_) {
+                                       long long slice_, bool direct_ = false) {
     n = n_;
     r = r_;
+    direct = direct_;
     lo = lo_;
     chCount = chCount_;
     K = K_;
@@ -61,13 +69,13 @@ struct RingIter {
       flags = F_IN | F_RECV | F_SEND;
     } else if (p == n - 1) {
       c = r;
-      flags = F_IN | F_RECV | F_POST | F_OUT | F_SEND;
+      flags = F_IN | F_RECV | F_POST | F_OUT | (direct ? F_DSEND : F_SEND);
     } else if (p <= 2 * n - 3) {
       c = ((r - (p - n + 1)) % n + n) % n;
-      flags = F_RECV | F_OUT | F_SEND;
+      flags = direct ? (F_DRECV | F_DSEND) : (F_RECV | F_OUT | F_SEND);
     } else {
       c = (r + 1) % n;
-      flags = F_RECV | F_OUT;
+      flags = direct ? F_DRECV : (F_RECV | F_OUT);  // direct: the data is already in place
     }
     const long long cLo = min(rem, (long long)c * k);
     cHi = off + min(rem, (long long)(c + 1) * k);

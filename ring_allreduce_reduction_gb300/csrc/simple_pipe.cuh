@@ -77,7 +77,10 @@ __device__ __forceinline__ void drainStages(const DevComm& c, unsigned long long
   }
 }
 
-template <int DT, int OP, bool TREE, class Args, class It>
+// DIRECT: the ring's all-gather through the recv buffers (F_DRECV /
+// F_DSEND slices); a separate instantiation, so the FIFO form carries none
+// of its per-slice work.
+template <int DT, int OP, bool TREE, bool DIRECT = false, class Args, class It>
 __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, char* out) {
   using S = typename Ty<DT>::S;
   constexpr int E = sizeof(S);
@@ -153,7 +156,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
     // in-edge slot is filled (cached flag values cover several slices per
     // poll), then bulk-copy the received slot(s) into the stage.
     if (lane != 0) return;
-    unsigned long long headSeen[2] = {0, 0}, tailSeen[2] = {0, 0};
+    unsigned long long headSeen[2] = {0, 0}, tailSeen[2] = {0, 0}, dtailSeen = 0;
     int lastUse[kMaxStages];
     for (int i = 0; i < NST; ++i) lastUse[i] = -1;
     SliceDesc d;
@@ -186,12 +189,28 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
           bulkLoad(buf + size_t(1 + i) * sliceBytes, ag.slot(c, ag.re[i], ag.rstep[i]), rvBytes, &sh.fullFifo[st]);
         }
       }
+      if (DIRECT && ok && (d.flags & F_DRECV) && (d.flags & F_DSEND)) {
+        // Direct: the predecessor wrote this slice into this rank's recv
+        // buffer; take its whole 16-byte units (the ragged end of the
+        // buffer is read element by element, never past the buffer).
+        const unsigned long long before = dtailSeen;
+        ok = flagAtLeast(c, ag, &c.dctrl[ag.dre].tail, ag.drstep + 1, dtailSeen, 0);
+        const unsigned dBytes = unsigned(d.nelem * E / 16 * 16);
+        if (ok && dBytes) {
+          if (dtailSeen != before) fenceProxyAsync();
+          lastUse[st] = use;
+          mbarExpectTx(&sh.fullFifo[st], dBytes);
+          bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes + sliceBytes, out + d.outPos * E, dBytes,
+                   &sh.fullFifo[st]);
+        }
+      }
       // On failure the consumers are told before this arrival, so the stage
       // it may complete is never published.
       if (!ok) *reinterpret_cast<volatile int*>(&sh.abort) = 1;
       mbarArrive(&sh.fullFifo[st]);
       if (!ok) break;
       ag.advance(d.flags);
+      if constexpr (DIRECT) ag.advanceDirect(d.flags);
       ++q;
     }
     if (!ok) {
@@ -225,19 +244,28 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
         continue;
       }
       bool send = false, recv = false;
+      int anyDirect = 0;
       while (more && q < (long long)done) {
         send |= (d.flags & F_SEND) != 0;
         recv |= (d.flags & F_RECV) != 0;
         ag.advance(d.flags);
+        if constexpr (DIRECT) {
+          anyDirect |= d.flags;
+          ag.advanceDirect(d.flags);
+        }
         ++q;
         more = it.next(d);
       }
-      if (send || recv) {
+      if (send || recv || (DIRECT && (anyDirect & (F_DSEND | F_DRECV)))) {
         fenceAcqRelGpu();
         if (send)
           for (int i = 0; i < ag.nsend; ++i) redMaxRelaxed(&c.ctrl[kSimple][ag.se[i]].tail, ag.sstep[i]);
         if (recv)
           for (int i = 0; i < ag.nrecv; ++i) redMaxRelaxed(&c.ctrl[kSimple][ag.re[i]].head, ag.rstep[i]);
+        if constexpr (DIRECT) {
+          if (anyDirect & F_DSEND) redMaxRelaxed(&c.dctrl[ag.dse].tail, ag.dsstep);
+          if (anyDirect & F_DRECV) redMaxRelaxed(&c.dctrl[ag.dre].head, ag.drstep);
+        }
       }
     }
     return;
@@ -246,6 +274,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
   // -------------------------------------------------------------- consumers
   const int ct = threadIdx.x - 96, CT = W * 32;
   const int cw = warp - 3;
+  char* const nextOut = DIRECT ? reinterpret_cast<char*>(a.recv[(ag.rank + 1) % a.nranks]) : nullptr;
   SliceDesc d;
   long long q = 0;
   while (it.next(d)) {
@@ -259,31 +288,37 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
     const char* sR0 = buf + sliceBytes;
     const char* sR1 = buf + 2 * sliceBytes;
     const bool rv = (d.flags & F_RECV) && ag.nrecv > 0;
+    const bool drv = DIRECT && (d.flags & F_DRECV) && (d.flags & F_DSEND);  // staged from own recv buffer
+    const int rf = d.flags | (drv ? F_RECV : 0);  // the reduction sees a received value
     char* dst0 = (d.flags & F_SEND) && ag.nsend > 0 ? ag.slot(c, ag.se[0], ag.sstep[0]) : nullptr;
     char* dst1 = (d.flags & F_SEND) && ag.nsend > 1 ? ag.slot(c, ag.se[1], ag.sstep[1]) : nullptr;
+    char* dnx = DIRECT && (d.flags & F_DSEND) ? nextOut + d.outPos * E : nullptr;
     char* o = out + d.outPos * E;
     const int nv = d.nelem / V;
     for (int i = ct; i < nv; i += CT) {
       const size_t b = size_t(i) * 16;
       uint4 xv = make_uint4(0, 0, 0, 0), r0v = xv, r1v = xv;
       if (d.flags & F_IN) xv = *reinterpret_cast<const uint4*>(sIn + b);
-      if (rv) r0v = *reinterpret_cast<const uint4*>(sR0 + b);
+      if (rv || drv) r0v = *reinterpret_cast<const uint4*>(sR0 + b);
       if (rv && ag.nrecv > 1) r1v = *reinterpret_cast<const uint4*>(sR1 + b);
       uint32_t x[4] = {xv.x, xv.y, xv.z, xv.w}, r0[4] = {r0v.x, r0v.y, r0v.z, r0v.w},
                r1[4] = {r1v.x, r1v.y, r1v.z, r1v.w}, acc[4];
-      reduceWords<DT, OP, TREE, 4>(acc, x, r0, r1, d.flags, ag.nrecv, a.scale, a.nranks);
+      reduceWords<DT, OP, TREE, 4>(acc, x, r0, r1, rf, ag.nrecv, a.scale, a.nranks);
       const uint4 av = make_uint4(acc[0], acc[1], acc[2], acc[3]);
       if (dst0) stFifo16(dst0 + b, av);
       if (dst1) stFifo16(dst1 + b, av);
+      if constexpr (DIRECT)
+        if (dnx) stFifo16(dnx + b, av);
       if (d.flags & F_OUT) stStream16(o + b, av);
     }
     for (int j = nv * V + ct; j < d.nelem; j += CT) {  // ragged end of the user buffer
       S x = (d.flags & F_IN) ? reinterpret_cast<const S*>(in + d.inPos * E)[j] : S(0);
-      S r0 = rv ? reinterpret_cast<const S*>(sR0)[j] : S(0);
+      S r0 = rv ? reinterpret_cast<const S*>(sR0)[j] : drv ? reinterpret_cast<const S*>(o)[j] : S(0);
       S r1 = (rv && ag.nrecv > 1) ? reinterpret_cast<const S*>(sR1)[j] : S(0);
-      S v = reduceElem<DT, OP, TREE>(x, r0, r1, d.flags, ag.nrecv, a.scale, a.nranks);
+      S v = reduceElem<DT, OP, TREE>(x, r0, r1, rf, ag.nrecv, a.scale, a.nranks);
       if (dst0) reinterpret_cast<S*>(dst0)[j] = v;
       if (dst1) reinterpret_cast<S*>(dst1)[j] = v;
+      if (dnx) reinterpret_cast<S*>(dnx)[j] = v;
       if (d.flags & F_OUT) reinterpret_cast<S*>(o)[j] = v;
     }
     if (rv) {
@@ -306,6 +341,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
                    : "memory");
     }
     ag.advance(d.flags);
+    if constexpr (DIRECT) ag.advanceDirect(d.flags);
     ++q;
   }
 }

@@ -104,6 +104,7 @@ struct vrcclComm {
   int envChannels;
   size_t envSliceBytes;
   int envWarps, envPrefetch;
+  bool direct;  // Simple ring AllReduce: all-gather through the recv buffers
   bool debug;
   bool haveLast;
   int lastAlgo, lastProto, lastChannels;
@@ -206,8 +207,10 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
     ok = cudaMalloc(&c->fifoAlloc[p], fifoBytes(p, nranks, nchannels)) == cudaSuccess &&
          cudaMemset(c->fifoAlloc[p], 0, fifoBytes(p, nranks, nchannels)) == cudaSuccess;
   }
-  ok = ok && cudaMalloc(&c->ctrlAlloc, nEdges * kNumProtos * sizeof(EdgeCtrl)) == cudaSuccess &&
-       cudaMemset(c->ctrlAlloc, 0, nEdges * kNumProtos * sizeof(EdgeCtrl)) == cudaSuccess;
+  // one control block per edge and protocol, then one per edge for the
+  // direct all-gather counters
+  ok = ok && cudaMalloc(&c->ctrlAlloc, nEdges * (kNumProtos + 1) * sizeof(EdgeCtrl)) == cudaSuccess &&
+       cudaMemset(c->ctrlAlloc, 0, nEdges * (kNumProtos + 1) * sizeof(EdgeCtrl)) == cudaSuccess;
   ok = ok && cudaMalloc(&c->statusAlloc, 256) == cudaSuccess && cudaMemset(c->statusAlloc, 0, 256) == cudaSuccess;
   ok = ok && cudaHostAlloc((void**)&c->hostAbortPinned, 64, cudaHostAllocMapped) == cudaSuccess;
   ok = ok && cudaStreamCreateWithFlags(&c->internal, cudaStreamNonBlocking) == cudaSuccess;
@@ -226,6 +229,7 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
     c->dc.fifo[p] = static_cast<char*>(c->fifoAlloc[p]);
     c->dc.ctrl[p] = static_cast<EdgeCtrl*>(c->ctrlAlloc) + p * nEdges;
   }
+  c->dc.dctrl = static_cast<EdgeCtrl*>(c->ctrlAlloc) + kNumProtos * nEdges;
   c->dc.status = static_cast<DevStatus*>(c->statusAlloc);
   c->dc.devAbort = reinterpret_cast<int*>(static_cast<char*>(c->statusAlloc) + 128);
   c->dc.hostAbort = devAbortHostView;
@@ -247,6 +251,7 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
   c->envSliceBytes = (size_t)std::max(0, envInt("VRCCL_SLICE_BYTES", 0)) / 16 * 16;
   c->envWarps = std::max(0, envInt("VRCCL_SIMPLE_WARPS", 0));
   c->envPrefetch = std::min(kMaxPrefetch, std::max(0, envInt("VRCCL_PREFETCH", 0)));
+  c->direct = envInt("VRCCL_DIRECT", 0) != 0;
   c->tuner.loadEnvFile(nranks);
   {
     std::lock_guard<std::mutex> lk(gLiveMu);
@@ -280,6 +285,12 @@ extern "C" vrcclResult_t vrcclCommSetSchedule(vrcclComm_t comm, int nchannels, s
   if (chunkBytes % 16) return vrcclInvalidArgument;
   comm->forceChannels = nchannels;
   comm->forceChunkBytes = chunkBytes;
+  return vrcclSuccess;
+}
+
+extern "C" vrcclResult_t vrcclCommSetDirect(vrcclComm_t comm, int enable) {
+  if (!validComm(comm) || (enable != 0 && enable != 1)) return vrcclInvalidArgument;
+  comm->direct = enable != 0;
   return vrcclSuccess;
 }
 
@@ -735,6 +746,7 @@ static vrcclResult_t runCall(vrcclComm_t comm, const Call& k) {
   ka.scale = 1.0f / (float)n;
   ka.stages = s.stages;
   ka.prefetch = s.P == kSimple ? comm->envPrefetch : 0;
+  ka.direct = comm->direct && s.A == kRing && s.P == kSimple && k.coll == kAllReduce && n > 1;
   for (int r = 0; r < n; ++r) {
     ka.send[r] = k.send[r];
     ka.recv[r] = k.recv[r];

@@ -17,6 +17,9 @@
 //                "NCCL Source Code Deep Dive", §2.4). tail = slots the sender
 //                has filled, head = slots the receiver has drained; both
 //                only grow, across launches.
+//   dctrl        one EdgeCtrl per ring edge for the "direct" all-gather:
+//                tail = slices the sender wrote straight into the
+//                receiver's recv buffer, head = slices the receiver took.
 //   status       first device-side failure (code, rank, channel, step).
 //   devAbort     set by the first agent that fails; every wait polls it.
 //   hostAbort    mapped pinned host word raised by vrcclCommAbort.
@@ -88,6 +91,7 @@ struct DevStatus {
 struct DevComm {
   char* fifo[kNumProtos];
   EdgeCtrl* ctrl[kNumProtos];
+  EdgeCtrl* dctrl;  // direct ring edges: tail = slices written into the next rank's recv buffer
   DevStatus* status;
   int* devAbort;
   volatile int* hostAbort;
@@ -110,6 +114,7 @@ struct KArgs {
   float scale;     // avg pre-scale 1.0f / n (binary32)
   int stages;      // Simple: shared-memory stages of the slice pipeline
   int prefetch;    // Simple: input slices pulled into L2 ahead of their stage (0 = off)
+  int direct;      // Simple ring AllReduce: all-gather through the peers' recv buffers
   const void* send[kMaxRanks];
   void* recv[kMaxRanks];
 };

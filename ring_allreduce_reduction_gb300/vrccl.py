@@ -55,6 +55,7 @@ _sig = {
     "vrcclModelPredict": [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_size_t, ctypes.c_int,
                           ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
                           ctypes.POINTER(ctypes.c_float)],
+    "vrcclCommSetDirect": [ctypes.c_void_p, ctypes.c_int],
     "vrcclCommSetSchedule": [ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t],
     "vrcclCommGetLastSchedule": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p, ctypes.POINTER(ctypes.c_size_t)],
     "vrcclCommGetAsyncError": [ctypes.c_void_p, _c_int_p],
@@ -203,6 +204,10 @@ def vrcclModelPredict(nranks: int, nnodes: int, nchannels: int, bw_intra: float,
                                   num_pipe_ops, ctypes.byref(lat), ctypes.byref(bw), ctypes.byref(t)),
            "vrcclModelPredict")
     return {"lat_us": lat.value, "algbw_gbs": bw.value, "time_us": t.value}
+
+
+def vrcclCommSetDirect(comm, enable: bool) -> None:
+    _check(_lib.vrcclCommSetDirect(comm, 1 if enable else 0), "vrcclCommSetDirect")
 
 
 def vrcclCommSetSchedule(comm, nchannels: int = 0, chunkBytes: int = 0) -> None:

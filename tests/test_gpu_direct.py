@@ -1,0 +1,122 @@
+"""GPU parity of the direct all-gather (vrcclCommSetDirect): the ring /
+Simple AllReduce whose all-gather moves through the ranks' recv buffers
+must give the oracle's bits, and the FIFO form's, for every type, op, rank
+count, ragged end and in place; switching between the two forms on one
+communicator must keep both correct."""
+import numpy as np
+import pytest
+
+from oracle import closed_form, ring as oring
+from ring_allreduce_reduction_gb300.workloads import ELEM_SIZE, make_inputs
+from tests.gpu_harness import run
+
+pytestmark = pytest.mark.gpu
+
+DT = ["int32", "float32", "bfloat16", "float16"]
+OPS = ["sum", "prod", "max", "min", "avg"]
+
+
+@pytest.fixture(scope="module")
+def v():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ring_allreduce_reduction_gb300 import build
+    build.build()
+    from ring_allreduce_reduction_gb300 import vrccl
+    return vrccl
+
+
+def _inputs(n, count, dtype, op, seed=0):
+    if dtype == "int32":
+        return make_inputs(n, count, dtype, "int_uniform", seed=seed, lo=-2**20, hi=2**20)
+    if op == "prod":
+        return make_inputs(n, count, dtype, "uniform", seed=seed, lo=0.5, hi=2.0)
+    return make_inputs(n, count, dtype, "normal", seed=seed)
+
+
+def _same(a, b):
+    return np.array_equal(np.ascontiguousarray(a).view(np.uint8), np.ascontiguousarray(b).view(np.uint8))
+
+
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_direct_every_dtype_and_op(v, n):
+    """3 channels, 256-byte chunks: several loops, a short last loop, a
+    ragged end shorter than 16 bytes."""
+    comm = v.vrcclCommInit(n, 4)
+    try:
+        v.vrcclCommSetSchedule(comm, 3, 256)
+        v.vrcclCommSetDirect(comm, True)
+        for dtype in DT:
+            count = 3001 if ELEM_SIZE[dtype] == 4 else 6003
+            for op in OPS:
+                x = _inputs(n, count, dtype, op, seed=n + len(op))
+                y, s, b = run(v, comm, x, dtype, op, "ring", "simple")
+                ref = oring.ring_allreduce(x, op, dtype, s["nchannels"], s["chunk_elems"])
+                assert _same(y, ref), (dtype, op)
+                ok, worst = closed_form.check(y[0], x, op, dtype)
+                assert ok, worst
+                assert b.canaries_intact()
+        assert v.vrcclCommGetAsyncError(comm) == 0
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("count", [1, 4, 7, 4096, 65536 * 3 + 5])
+def test_direct_inplace_and_mode_switches(v, count):
+    n = 6
+    comm = v.vrcclCommInit(n, 8)
+    try:
+        for it, (direct, inplace) in enumerate([(True, False), (True, True), (False, True), (True, False),
+                                                (False, False), (True, True)]):
+            v.vrcclCommSetDirect(comm, direct)
+            x = _inputs(n, count, "bfloat16", "sum", seed=it)
+            y, s, b = run(v, comm, x, "bfloat16", "sum", "ring", "simple", inplace=inplace)
+            ref = oring.ring_allreduce(x, "sum", "bfloat16", s["nchannels"], s["chunk_elems"])
+            assert _same(y, ref), (it, direct, inplace)
+            assert b.canaries_intact()
+        assert v.vrcclCommGetAsyncError(comm) == 0
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("n", [16, 32])
+def test_direct_many_ranks(v, n):
+    comm = v.vrcclCommInit(n, 8)
+    try:
+        v.vrcclCommSetDirect(comm, True)
+        x = _inputs(n, 300_001, "float32", "sum", seed=n)
+        y, s, b = run(v, comm, x, "float32", "sum", "ring", "simple")
+        ref = oring.ring_allreduce(x, "sum", "float32", s["nchannels"], s["chunk_elems"])
+        assert _same(y, ref) and b.canaries_intact()
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+def test_direct_full_size_matches_fifo_form(v):
+    """The bench workload (n=8, 256 MiB fp32 per rank): the direct and FIFO
+    forms give the same 2 GiB of results, compared on the device; sampled
+    outputs match the oracle's predictor."""
+    import torch
+    n, count = 8, (256 << 20) // 4
+    x = make_inputs(n, count, "float32", "uniform", seed=1000)
+    send = torch.from_numpy(x).to("cuda:0")
+    r1 = torch.empty_like(send)
+    r2 = torch.empty_like(send)
+    comm = v.vrcclCommInit(n, 32)
+    try:
+        v.vrcclAllReduce([send[r] for r in range(n)], [r1[r] for r in range(n)], count, "float32", "sum", "ring",
+                         "simple", comm)
+        s1 = v.vrcclCommGetLastSchedule(comm)
+        v.vrcclCommSetDirect(comm, True)
+        v.vrcclAllReduce([send[r] for r in range(n)], [r2[r] for r in range(n)], count, "float32", "sum", "ring",
+                         "simple", comm)
+        torch.cuda.synchronize()
+        assert v.vrcclCommGetLastSchedule(comm) == s1
+        assert v.vrcclCommGetAsyncError(comm) == 0
+        assert torch.equal(r1.view(torch.int32), r2.view(torch.int32))
+        idx = np.unique(np.concatenate([np.random.default_rng(9).choice(count, 100_000, replace=False),
+                                        [0, count - 1]]))
+        got = r2[3].cpu().numpy()[idx]
+        assert _same(got, oring.ring_predict(x, "sum", "float32", s1["nchannels"], s1["chunk_elems"], idx))
+    finally:
+        v.vrcclCommDestroy(comm)
