@@ -559,10 +559,13 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
     // Shrink the agent first, then (if the caller left it open) the channels.
     const int nbuf = A == kTree ? 3 : 2;
     SimpleShape sh;
-    // 2-byte types do twice the element arithmetic per byte: their consumers
-    // need twice the warps to keep up (measured on the bf16 avg bucket:
-    // 8 warps 6.2 ms, 16 warps 5.1 ms; fp32 is 2 % slower with 16).
-    const int maxWarps = comm->envWarps ? std::min(comm->envWarps, kMaxConsumerWarps) : (kE == 2 ? 16 : 8);
+    // 2-byte types do twice the element arithmetic per byte: with a large
+    // share per agent their consumers need twice the warps to keep up
+    // (measured on the bf16 avg bucket: 8 warps 6.2 ms, 16 warps 5.1 ms;
+    // fp32 is 2 % slower with 16). Below 1 MiB per agent the larger block
+    // only adds latency (bf16 1 KiB: 41 us with 8 warps, 49 us with 16).
+    const bool wide = kE == 2 && bytes / std::max(C, 1) >= (size_t(1) << 20);
+    const int maxWarps = comm->envWarps ? std::min(comm->envWarps, kMaxConsumerWarps) : (wide ? 16 : 8);
     while (!pickSimpleShape(comm, fn, per * C, nbuf, wantSlice, maxWarps, &sh)) {
       if (userChannels || C == 1) return userAlgo || userChannels ? vrcclInvalidUsage : vrcclInternalError;
       --C;
