@@ -278,7 +278,7 @@ __device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int
 
 // ------------------------------------------------------------------- LL128
 // A 128-byte line is eight 16-byte pieces held by eight lanes of a warp; a
-// warp moves four lines per pass. Pieces 0..6 carry 16 user bytes, piece 7
+// warp moves four groups of four lines per pass. Pieces 0..6 carry 16 user bytes, piece 7
 // carries 8 user bytes and, in its upper half, the 8-byte flag
 // (step + 1); line L of a slice carries user bytes [120 L, 120 L + 120).
 //
@@ -289,50 +289,56 @@ __device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int
 // the other lanes' data stores before it, and the reader's flag lane polls
 // with acquire loads and the warp barrier orders the data loads after it.
 // The line format and its 93.75 % payload are unchanged.
-template <int DT, int OP, bool TREE, class Args>
-__device__ bool llSlice128(const Args& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
+// The passes of one LL128 slice with U groups of four lines per warp and
+// pass; returns false if a wait gave up.
+template <int U, int DT, int OP, bool TREE, class Args>
+__device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char* in, char* out, int nbytes,
+                                            int nlines, int flags, const char* const* src, char* const* dst) {
   using S = typename Ty<DT>::S;
-  __shared__ int smFail;
+  constexpr int NR = TREE ? 2 : 1;    // in-edges
   const DevComm& c = a.comm;
-  if (!slicePrologue(c, ag, flags, false, &smFail)) return false;
-
-  const int nbytes = nelem * int(sizeof(S));
-  const int nlines = (nbytes + kLL128DataBytes - 1) / kLL128DataBytes;
   const bool rv = (flags & F_RECV) && ag.nrecv > 0;
-  const char* src[2] = {nullptr, nullptr};
-  if (rv)
-    for (int i = 0; i < ag.nrecv; ++i) src[i] = ag.slot(c, ag.re[i], ag.rstep[i]);
-  char* dst[2] = {nullptr, nullptr};
-  if (flags & F_SEND)
-    for (int i = 0; i < ag.nsend; ++i) dst[i] = ag.slot(c, ag.se[i], ag.sstep[i]);
-
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int p = lane & 7;
-  const int pieceBytes = p < 7 ? 16 : 8;
+  const int p = lane & 7;     // piece of the line this lane moves
+  const int k = lane >> 3;    // line within a group of four
   bool fail = false;
-  for (int g = warp * 4; g < nlines; g += nwarps * 4) {
-    const int line = g + (lane >> 3);
-    const bool active = line < nlines;
-    const int ub = line * kLL128DataBytes + p * 16;  // first user byte of this piece
-    const int valid0 = active ? max(0, min(8, nbytes - ub)) : 0;
-    const int valid1 = (active && p < 7) ? max(0, min(8, nbytes - ub - 8)) : 0;
-    uint32_t x[4] = {0u, 0u, 0u, 0u};
-    if ((flags & F_IN) && valid0 > 0) {
-      uint2 u0 = loadUnit<S>(in + ub, valid0);
-      x[0] = u0.x;
-      x[1] = u0.y;
-      if (valid1 > 0) {
-        uint2 u1 = loadUnit<S>(in + ub + 8, valid1);
-        x[2] = u1.x;
-        x[3] = u1.y;
+  // A pass covers lines g0 + 4u + k (u < U). Lane p = 7 - u of group k also
+  // polls (and, sending, releases) the flag of line g0 + 4u + k, so a pass's
+  // flags are waited on and published by as many lanes at once; u = 0 is
+  // the lane that holds the flag's piece itself.
+  for (int g0 = warp * 4 * U; g0 < nlines; g0 += nwarps * 4 * U) {
+    int ub[U], valid0[U], valid1[U];
+    uint32_t x[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int line = g0 + 4 * u + k;
+      const bool active = line < nlines;
+      ub[u] = line * kLL128DataBytes + p * 16;  // first user byte of this piece
+      valid0[u] = active ? max(0, min(8, nbytes - ub[u])) : 0;
+      valid1[u] = (active && p < 7) ? max(0, min(8, nbytes - ub[u] - 8)) : 0;
+      x[u][0] = x[u][1] = x[u][2] = x[u][3] = 0u;
+      if ((flags & F_IN) && valid0[u] > 0) {
+        const uint2 u0 = loadUnit<S>(in + ub[u], valid0[u]);
+        x[u][0] = u0.x;
+        x[u][1] = u0.y;
+        if (valid1[u] > 0) {
+          const uint2 u1 = loadUnit<S>(in + ub[u] + 8, valid1[u]);
+          x[u][2] = u1.x;
+          x[u][3] = u1.y;
+        }
       }
     }
-    uint32_t r[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+    uint32_t r[U][NR][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < NR; ++i) r[u][i][0] = r[u][i][1] = r[u][i][2] = r[u][i][3] = 0u;
     if (rv) {
-      if (active && p == 7) {
+      const int pl = g0 + 4 * (7 - p) + k;  // the line whose flag this lane waits for
+      if (7 - p < U && pl < nlines) {
         for (int i = 0; i < ag.nrecv && !fail; ++i) {
           const unsigned long long* flagp =
-              reinterpret_cast<const unsigned long long*>(src[i] + size_t(line) * 128 + 120);
+              reinterpret_cast<const unsigned long long*>(src[i] + size_t(pl) * 128 + 120);
           const unsigned long long want = ag.rstep[i] + 1;
           Spin sp;
           while (ldAcquire(flagp) != want) {
@@ -347,42 +353,74 @@ __device__ bool llSlice128(const Args& a, Agent& ag, const char* in, char* out, 
         fail = true;
         break;
       }
-      __syncwarp();
-      if (active) {
-        for (int i = 0; i < ag.nrecv; ++i) {
-          const char* lp = src[i] + size_t(line) * 128 + p * 16;
+      __syncwarp();  // every flag of the pass seen: the lines are complete
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (g0 + 4 * u + k >= nlines) continue;
+        for (int i = 0; i < ag.nrecv && i < NR; ++i) {
+          const char* lp = src[i] + size_t(g0 + 4 * u + k) * 128 + p * 16;
           if (p < 7) {
-            uint4 v = ldFifo16(lp);
-            r[i][0] = v.x; r[i][1] = v.y; r[i][2] = v.z; r[i][3] = v.w;
+            const uint4 v = ldFifo16(lp);
+            r[u][i][0] = v.x; r[u][i][1] = v.y; r[u][i][2] = v.z; r[u][i][3] = v.w;
           } else {
-            uint2 v = ldFifo8(lp);
-            r[i][0] = v.x; r[i][1] = v.y;
+            const uint2 v = ldFifo8(lp);
+            r[u][i][0] = v.x; r[u][i][1] = v.y;
           }
         }
       }
     }
-    uint32_t acc[4];
-    reduceWords<DT, OP, TREE, 4>(acc, x, r[0], r[1], flags, ag.nrecv, a.scale, a.nranks);
+    uint32_t acc[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      reduceWords<DT, OP, TREE, 4>(acc[u], x[u], r[u][0], r[u][NR - 1], flags, ag.nrecv, a.scale, a.nranks);
     if (flags & F_SEND) {
-      if (active) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (g0 + 4 * u + k >= nlines) continue;
         for (int i = 0; i < ag.nsend; ++i) {
-          char* lp = dst[i] + size_t(line) * 128 + p * 16;
-          if (p < 7) stFifo16(lp, make_uint4(acc[0], acc[1], acc[2], acc[3]));
-          else stFifo8(lp, make_uint2(acc[0], acc[1]));
+          char* lp = dst[i] + size_t(g0 + 4 * u + k) * 128 + p * 16;
+          if (p < 7) stFifo16(lp, make_uint4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]));
+          else stFifo8(lp, make_uint2(acc[u][0], acc[u][1]));
         }
       }
-      __syncwarp();
-      if (active && p == 7)
+      __syncwarp();  // the pass's data stores before its flags
+      const int pl = g0 + 4 * (7 - p) + k;
+      if (7 - p < U && pl < nlines)
         for (int i = 0; i < ag.nsend; ++i)
-          stRelease(reinterpret_cast<unsigned long long*>(dst[i] + size_t(line) * 128 + 120), ag.sstep[i] + 1);
+          stRelease(reinterpret_cast<unsigned long long*>(dst[i] + size_t(pl) * 128 + 120), ag.sstep[i] + 1);
     }
-    if ((flags & F_OUT) && valid0 > 0) {
-      storeUnit<S>(out + ub, make_uint2(acc[0], acc[1]), valid0);
-      if (valid1 > 0) storeUnit<S>(out + ub + 8, make_uint2(acc[2], acc[3]), valid1);
+    if (flags & F_OUT) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (valid0[u] > 0) storeUnit<S>(out + ub[u], make_uint2(acc[u][0], acc[u][1]), valid0[u]);
+        if (valid1[u] > 0) storeUnit<S>(out + ub[u] + 8, make_uint2(acc[u][2], acc[u][3]), valid1[u]);
+      }
     }
-    (void)pieceBytes;
   }
-  if (fail && lane == 0) smFail = 1;
+  return !fail;
+}
+
+template <int U, int DT, int OP, bool TREE, class Args>
+__device__ bool llSlice128(const Args& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
+  using S = typename Ty<DT>::S;
+  __shared__ int smFail;
+  const DevComm& c = a.comm;
+  if (!slicePrologue(c, ag, flags, false, &smFail)) return false;
+  const int nbytes = nelem * int(sizeof(S));
+  const int nlines = (nbytes + kLL128DataBytes - 1) / kLL128DataBytes;
+  const bool rv = (flags & F_RECV) && ag.nrecv > 0;
+  const char* src[2] = {nullptr, nullptr};
+  if (rv)
+    for (int i = 0; i < ag.nrecv; ++i) src[i] = ag.slot(c, ag.re[i], ag.rstep[i]);
+  char* dst[2] = {nullptr, nullptr};
+  if (flags & F_SEND)
+    for (int i = 0; i < ag.nsend; ++i) dst[i] = ag.slot(c, ag.se[i], ag.sstep[i]);
+  // U = 4 (the wide kernels, for long slices): more loads and flags in
+  // flight per warp; U = 1: the shortest chain per line. The two live in
+  // different kernels: the four-group code in the same kernel measured
+  // slower on short slices (ring LL128, bf16 16 KiB: 37 -> 49 us).
+  const bool ok = ll128Passes<U, DT, OP, TREE>(a, ag, in, out, nbytes, nlines, flags, src, dst);
+  if (!ok && (threadIdx.x & 31) == 0) smFail = 1;
   __syncthreads();
   if (smFail) return false;
   if (threadIdx.x == 0 && rv)
@@ -395,7 +433,8 @@ template <int PROTO, int DT, int OP, bool TREE, class Args>
 __device__ __forceinline__ bool runSlice(const Args& a, Agent& ag, const char* in, char* out, int nelem,
                                          int flags) {
   if constexpr (PROTO == kLL) return llSlice<DT, OP, TREE>(a, ag, in, out, nelem, flags);
-  if constexpr (PROTO == kLL128) return llSlice128<DT, OP, TREE>(a, ag, in, out, nelem, flags);
+  if constexpr (PROTO == kLL128) return llSlice128<1, DT, OP, TREE>(a, ag, in, out, nelem, flags);
+  if constexpr (PROTO == kLL128Wide) return llSlice128<4, DT, OP, TREE>(a, ag, in, out, nelem, flags);
 }
 
 }  // namespace vrccl

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) ringKernel(const __gri
   char* out = reinterpret_cast<char*>(a.recv[r]);
 
   Agent ag;
-  ag.init(c, PROTO, r, ch);
+  ag.init(c, wireProto(PROTO), r, ch);
   if (n > 1) {
     ag.addRecv(c, ringEdge(ch, (r - 1 + n) % n, n));
     ag.addSend(c, ringEdge(ch, r, n));
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) treeKernel(const __gri
   const int maxCh = c.maxChannels;
 
   Agent ag;
-  ag.init(c, PROTO, rank, ch);
+  ag.init(c, wireProto(PROTO), rank, ch);
   int flags;
   if (!downRole) {
     if (d0 >= 0) ag.addRecv(c, treeUpEdge(ch, d0, n, maxCh));

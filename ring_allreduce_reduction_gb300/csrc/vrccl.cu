@@ -31,6 +31,8 @@ extern const void* const kRingLL[4][5];
 extern const void* const kTreeLL[4][5];
 extern const void* const kRingLL128[4][5];
 extern const void* const kTreeLL128[4][5];
+extern const void* const kRingLL128W[4][5];
+extern const void* const kTreeLL128W[4][5];
 extern const void* const kOneShot[4][5];
 extern const void* const kGroupSimple[4][5];
 extern const void* const kGroupLL[4][5];
@@ -55,6 +57,8 @@ const void* kernelFor(int algo, int proto, int dtype, int op) {
     case kLL * 2 + kTree: return kTreeLL[dtype][op];
     case kLL128 * 2 + kRing: return kRingLL128[dtype][op];
     case kLL128 * 2 + kTree: return kTreeLL128[dtype][op];
+    case kLL128Wide * 2 + kRing: return kRingLL128W[dtype][op];
+    case kLL128Wide * 2 + kTree: return kTreeLL128W[dtype][op];
   }
   return nullptr;
 }
@@ -531,7 +535,10 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
         : (ch.channels > 0 ? std::min(ch.channels, comm->maxChannels)
                            : defaultChannels(P, bytes, n, comm->maxChannels));
   const bool userChannels = comm->forceChannels || comm->envChannels;
-  const void* fn = grouped ? groupKernelFor(P, kdtype, kop) : kernelFor(A, P, kdtype, kop);
+  // LL128 with at least two whole slices per agent takes the wide kernels.
+  const size_t perAgent = bytes / std::max(C, 1) / (A == kRing ? n : 1);
+  const int kp = P == kLL128 && !grouped && perAgent >= 2 * slotDataBytes(kLL128) ? kLL128Wide : P;
+  const void* fn = grouped ? groupKernelFor(P, kdtype, kop) : kernelFor(A, kp, kdtype, kop);
   if (!fn) return vrcclInternalError;
   const int per = agentsPerChannel(A, n);
   if (!userChannels && ch.channels == 0 && per * C > comm->smCount) {

@@ -42,6 +42,10 @@ constexpr int kMaxRanks = VRCCL_MAX_RANKS;
 constexpr int kNumProtos = 3;
 
 enum ProtoId { kSimple = 0, kLL = 1, kLL128 = 2 };
+// Kernel variant, not a wire protocol: LL128 moving four groups of lines per
+// warp and pass (long slices). Same lines, flags and FIFOs as kLL128.
+constexpr int kLL128Wide = 3;
+__host__ __device__ constexpr int wireProto(int kernelProto) { return kernelProto == kLL128Wide ? kLL128 : kernelProto; }
 enum AlgoId { kRing = 0, kTree = 1 };
 // What one launch computes: the AllReduce, or one of its two ring phases
 // run alone (ReduceScatter, AllGather).
@@ -57,8 +61,10 @@ constexpr int kMaxConsumerWarps = 16;  // Simple: 3 service warps + up to 16 con
 // Thread bound a kernel is compiled for. A Simple agent has at most 3 + 16
 // warps (608 threads); its bound of 736 threads caps registers at 65536 / 736
 // = 89 per thread, so two 352-thread agents (8 consumer warps) still fit on
-// one SM without spilling. LL / LL128 agents use up to 1024 threads.
-__host__ __device__ constexpr int maxAgentThreads(int proto) { return proto == 0 ? 736 : 1024; }
+// one SM without spilling. LL / LL128 agents use at most 256 threads (the
+// host starts there and halves to fit), which leaves LL128's unrolled passes
+// their registers.
+__host__ __device__ constexpr int maxAgentThreads(int proto) { return proto == kSimple ? 736 : 256; }
 constexpr int kMaxPrefetch = 32;       // Simple: largest input L2 prefetch distance (slices)
 
 __host__ __device__ constexpr size_t slotBufferBytes(int proto) {

@@ -331,3 +331,24 @@ def test_two_byte_sums_on_hostile_values(v, dtype, op):
             assert b.canaries_intact()
     finally:
         v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("algo", ["ring", "tree"])
+def test_ll128_long_slices(v, algo):
+    """LL128 with several whole slices per agent (the wide kernels: four
+    groups of lines per warp and pass), every type and a ragged end."""
+    n = 5
+    comm = v.vrcclCommInit(n, 4)
+    try:
+        v.vrcclCommSetSchedule(comm, 2, 0)
+        for dtype, op in (("float32", "sum"), ("bfloat16", "avg"), ("float16", "max"), ("int32", "prod")):
+            count = 400_003 if ELEM_SIZE[dtype] == 4 else 800_011
+            x = _inputs(n, count, dtype, op, seed=count % 97)
+            for inplace in (False, True):
+                y, sched, b = run(v, comm, x, dtype, op, algo, "ll128", inplace=inplace)
+                assert sched["proto"] == "ll128" and sched["nchannels"] == 2
+                _assert_parity(x, y, dtype, op, sched)
+                assert b.canaries_intact()
+        assert v.vrcclCommGetAsyncError(comm) == 0
+    finally:
+        v.vrcclCommDestroy(comm)
