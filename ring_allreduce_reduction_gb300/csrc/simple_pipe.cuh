@@ -123,25 +123,26 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
       if (pmore && (pd.flags & F_IN) && pd.nelem * E >= 16) bulkPrefetchL2(in + pd.inPos * E, unsigned(pd.nelem * E / 16 * 16));
     }
     SliceDesc d;
-    long long q = 0;
+    int st = 0, ph = 0;  // next stage and its phase (no division per slice)
     bool ok = true;
     while (it.next(d)) {
-      const int st = (int)(q % NST);
-      const int use = (int)(q / NST);
       if (pmore && (pmore = ahead.next(pd)) && (pd.flags & F_IN) && pd.nelem * E >= 16)
         bulkPrefetchL2(in + pd.inPos * E, unsigned(pd.nelem * E / 16 * 16));
-      if (!pipeWait(c, ag, &sh, &sh.empty[st], (use & 1) ^ 1)) {
+      if (!pipeWait(c, ag, &sh, &sh.empty[st], ph ^ 1)) {
         ok = false;
         break;
       }
       const unsigned inBytes = (d.flags & F_IN) ? unsigned(d.nelem * E / 16 * 16) : 0u;
       if (inBytes) {
-        lastUse[st] = use;
+        lastUse[st] = ph;
         mbarExpectTx(&sh.fullIn[st], inBytes);
         bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes, in + d.inPos * E, inBytes, &sh.fullIn[st]);
       }
       mbarArrive(&sh.fullIn[st]);
-      ++q;
+      if (++st == NST) {
+        st = 0;
+        ph ^= 1;
+      }
     }
     if (!ok) {
       *reinterpret_cast<volatile int*>(&sh.abort) = 1;
@@ -160,12 +161,10 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
     int lastUse[kMaxStages];
     for (int i = 0; i < NST; ++i) lastUse[i] = -1;
     SliceDesc d;
-    long long q = 0;
+    int st = 0, ph = 0;  // next stage and its phase
     bool ok = true;
     while (it.next(d)) {
-      const int st = (int)(q % NST);
-      const int use = (int)(q / NST);
-      if (ag.faultNow(c) || !pipeWait(c, ag, &sh, &sh.empty[st], (use & 1) ^ 1)) {
+      if (ag.faultNow(c) || !pipeWait(c, ag, &sh, &sh.empty[st], ph ^ 1)) {
         ok = false;
         break;
       }
@@ -184,7 +183,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
           ok = flagAtLeast(c, ag, &c.ctrl[kSimple][ag.re[i]].tail, ag.rstep[i] + 1, tailSeen[i], 0);
           if (!ok) break;
           if (tailSeen[i] != before) fenceProxyAsync();
-          lastUse[st] = use;
+          lastUse[st] = ph;
           mbarExpectTx(&sh.fullFifo[st], rvBytes);
           bulkLoad(buf + size_t(1 + i) * sliceBytes, ag.slot(c, ag.re[i], ag.rstep[i]), rvBytes, &sh.fullFifo[st]);
         }
@@ -198,7 +197,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
         const unsigned dBytes = unsigned(d.nelem * E / 16 * 16);
         if (ok && dBytes) {
           if (dtailSeen != before) fenceProxyAsync();
-          lastUse[st] = use;
+          lastUse[st] = ph;
           mbarExpectTx(&sh.fullFifo[st], dBytes);
           bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes + sliceBytes, out + d.outPos * E, dBytes,
                    &sh.fullFifo[st]);
@@ -211,7 +210,10 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
       if (!ok) break;
       ag.advance(d.flags);
       if constexpr (DIRECT) ag.advanceDirect(d.flags);
-      ++q;
+      if (++st == NST) {
+        st = 0;
+        ph ^= 1;
+      }
     }
     if (!ok) {
       *reinterpret_cast<volatile int*>(&sh.abort) = 1;
@@ -276,12 +278,11 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
   const int cw = warp - 3;
   char* const nextOut = DIRECT ? reinterpret_cast<char*>(a.recv[(ag.rank + 1) % a.nranks]) : nullptr;
   SliceDesc d;
-  long long q = 0;
+  unsigned q = 0;      // slices done
+  int st = 0, ph = 0;  // stage and phase
   while (it.next(d)) {
-    const int st = (int)(q % NST);
-    const int use = (int)(q / NST);
-    if (!pipeWait(c, ag, &sh, &sh.fullIn[st], use & 1)) return;
-    if (!pipeWait(c, ag, &sh, &sh.fullFifo[st], use & 1)) return;
+    if (!pipeWait(c, ag, &sh, &sh.fullIn[st], ph)) return;
+    if (!pipeWait(c, ag, &sh, &sh.fullFifo[st], ph)) return;
     if (*reinterpret_cast<volatile int*>(&sh.abort)) return;
     const char* buf = smemDyn + size_t(st) * NBUF * sliceBytes;
     const char* sIn = buf;
@@ -337,11 +338,15 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
       // Free the stage (its shared memory has been read), then report the
       // slice done; the release orders this warp's stores before the report.
       mbarArrive(&sh.empty[st]);
-      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smemAddr(&sh.prog[cw])), "r"(unsigned(q + 1))
+      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smemAddr(&sh.prog[cw])), "r"(q + 1)
                    : "memory");
     }
     ag.advance(d.flags);
     if constexpr (DIRECT) ag.advanceDirect(d.flags);
+    if (++st == NST) {
+      st = 0;
+      ph ^= 1;
+    }
     ++q;
   }
 }
