@@ -552,6 +552,9 @@ def main() -> int:
                    "slice_elems": shape["slice_elems"],
                    "l2": "inputs larger than L2 (n*S = 2 GiB in, 2 GiB out); no flush",
                    "algbw_gbs": round(S / (ms_step / 1e3) / 1e9 * world, 3)},
+        "kernel_ms": {"p10": round(float(np.percentile(kern_ms, 10)), 4),
+                      "p50": round(float(np.percentile(kern_ms, 50)), 4),
+                      "p90": round(float(np.percentile(kern_ms, 90)), 4)},
         "roofline": roofline,
         "oneshot_bound": bound,
         "cpu_baseline": cpu,
