@@ -45,8 +45,32 @@ def time_call(v, comm, sp, rp, count, dtype, op, algo, proto, iters, warmup, str
     return e0.elapsed_time(e1) * 1e3 / iters
 
 
+def time_graph(v, comm, sp, rp, count, dtype, op, algo, proto, calls, reps, stream) -> float:
+    """Mean microseconds per call with `calls` calls captured in one CUDA
+    graph and the graph replayed `reps` times: the device-side latency,
+    without the host's launch overhead. (A replay does not run the host's
+    LL/LL128 flag-wrap accounting; `calls * reps` stays far below the 2^31
+    steps after which a flag could repeat.)"""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        cap = torch.cuda.current_stream()
+        for _ in range(calls):
+            v.vrcclAllReduce(sp, rp, count, dtype, op, algo, proto, comm, cap)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (calls * reps)
+
+
 def sweep(nranks: int, dtype: str, sizes: list[int], protos: list[str], algos: list[str], channels: list[int],
-          op: str = "sum", max_channels: int = 32, iters: int = 30, warmup: int = 3, log=print) -> list[dict]:
+          op: str = "sum", max_channels: int = 32, iters: int = 30, warmup: int = 3, log=print,
+          graph: bool = False) -> list[dict]:
     """Time every candidate at every size; returns one record per point."""
     from ring_allreduce_reduction_gb300 import vrccl as v
     E = ELEM[dtype]
@@ -74,6 +98,8 @@ def sweep(nranks: int, dtype: str, sizes: list[int], protos: list[str], algos: l
                         try:
                             it = iters if nbytes <= (1 << 24) else max(3, iters // 10)
                             us = time_call(v, comm, sp, rp, count, dtype, op, algo, proto, it, warmup, stream)
+                            if graph:  # the same point, 1000 calls per graph replay
+                                us = time_graph(v, comm, sp, rp, count, dtype, op, algo, proto, 1000, 3, stream)
                         except v.VrcclError as e:  # a shape this GPU cannot hold at once
                             log(f"# skip n={nranks} {algo}/{proto} C={nch} {nbytes} B: {e}")
                             continue
@@ -178,6 +204,8 @@ def main() -> int:
     ap.add_argument("--iters", type=int, default=30)
     ap.add_argument("--out", default="")
     ap.add_argument("--json", default="")
+    ap.add_argument("--graph", action="store_true",
+                    help="time 1000 calls captured in a CUDA graph per point (device latency, no launch overhead)")
     args = ap.parse_args()
     if args.compare:
         rows, graph = compare(read_table(args.compare))
@@ -189,7 +217,8 @@ def main() -> int:
         b *= 2
     t0 = time.time()
     recs = sweep(args.nranks, args.dtype, sizes, args.protos.split(","), args.algos.split(","),
-                 [int(c) for c in args.channels.split(",")], args.op, args.max_channels, args.iters)
+                 [int(c) for c in args.channels.split(",")], args.op, args.max_channels, args.iters,
+                 graph=args.graph)
     if args.out:
         write_table(recs, args.out, header=f"measured on {torch.cuda.get_device_name()} in {time.time() - t0:.0f} s, "
                                            f"dtype {args.dtype}, op {args.op}")
