@@ -43,7 +43,13 @@
  * defined after the stream is synchronised. Calls on one communicator
  * share its FIFOs: they must be ordered (one stream, or streams ordered by
  * events); calls that overlap on the GPU are undefined. Different
- * communicators are independent.
+ * communicators are independent. Calls may be captured in a CUDA graph:
+ * the FIFO counters and flags live in device memory and continue from one
+ * replay to the next, so a replayed call gives the same results as a
+ * direct one, provided the communicator's launches (captured or not) stay
+ * ordered. A replay does not run the host's LL flag-wrap accounting (the
+ * FIFOs are cleared before a 32-bit LL flag could repeat); that takes
+ * about 2^31 LL steps per ring edge, i.e. millions of replayed LL calls.
  *
  * Errors. Synchronous errors return a code and launch nothing. A device-
  * side failure (a wait that timed out, or an abort) is reported later by
