@@ -352,3 +352,25 @@ def test_ll128_long_slices(v, algo):
         assert v.vrcclCommGetAsyncError(comm) == 0
     finally:
         v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("proto", ["simple", "ll", "ll128"])
+@pytest.mark.parametrize("algo", ["ring", "tree"])
+def test_maximum_rank_count(v, algo, proto):
+    """n = VRCCL_MAX_RANKS (128): 255 primitives per ring loop, trees of
+    depth 7, a ragged count; one channel (a tree channel is 255 agents)."""
+    n = v.MAX_RANKS
+    comm = v.vrcclCommInit(n, 2)
+    try:
+        v.vrcclCommSetSchedule(comm, 1, 0)
+        x = _inputs(n, 5003, "float32", "sum", seed=128)
+        y, sched, b = run(v, comm, x, "float32", "sum", algo, proto)
+        assert sched["nchannels"] == 1
+        _assert_parity(x, y, "float32", "sum", sched)
+        assert b.canaries_intact()
+        xi = _inputs(n, 777, "int32", "avg", seed=129)
+        y, sched, b = run(v, comm, xi, "int32", "avg", algo, proto)
+        _assert_parity(xi, y, "int32", "avg", sched)
+        assert v.vrcclCommGetAsyncError(comm) == 0
+    finally:
+        v.vrcclCommDestroy(comm)
