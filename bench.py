@@ -490,6 +490,12 @@ def main() -> int:
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
                 "algorithmic_bytes_per_launch": algo_bytes}
+    if traffic:
+        # achieved DRAM GB/s: the ncu-measured DRAM bytes of one launch over
+        # the live mean launch time, against the measured and the nominal peak
+        dram = traffic / mean_kern_s / 1e9
+        roofline.update({"dram_gbs": round(dram, 1), "dram_frac": round(dram / peak, 4),
+                         "dram_frac_of_8tbs": round(dram / 8000.0, 4)})
 
     # ---- end to end through the public API with pinned host buffers
     e2e = None
