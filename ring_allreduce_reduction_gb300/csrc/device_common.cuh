@@ -108,6 +108,22 @@ __device__ __forceinline__ void bulkLoad(void* dstSmem, const void* srcGlobal, u
       "l"(srcGlobal), "r"(bytes), "r"(smemAddr(bar))
       : "memory");
 }
+// The same copy, tagged to be evicted from L2 first: for data read once
+// (an agent's own input), so it does not push out FIFO lines that are still
+// to be read.
+__device__ __forceinline__ unsigned long long evictFirstPolicy() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulkLoadOnce(void* dstSmem, const void* srcGlobal, unsigned bytes,
+                                             unsigned long long* bar, unsigned long long policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smemAddr(dstSmem)),
+      "l"(srcGlobal), "r"(bytes), "r"(smemAddr(bar)), "l"(policy)
+      : "memory");
+}
 // Starts pulling a global range into L2 (no destination in this SM).
 __device__ __forceinline__ void bulkPrefetchL2(const void* srcGlobal, unsigned bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(srcGlobal), "r"(bytes) : "memory");

@@ -125,6 +125,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
     SliceDesc d;
     int st = 0, ph = 0;  // next stage and its phase (no division per slice)
     bool ok = true;
+    const unsigned long long once = evictFirstPolicy();
     while (it.next(d)) {
       if (pmore && (pmore = ahead.next(pd)) && (pd.flags & F_IN) && pd.nelem * E >= 16)
         bulkPrefetchL2(in + pd.inPos * E, unsigned(pd.nelem * E / 16 * 16));
@@ -136,7 +137,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
       if (inBytes) {
         lastUse[st] = ph;
         mbarExpectTx(&sh.fullIn[st], inBytes);
-        bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes, in + d.inPos * E, inBytes, &sh.fullIn[st]);
+        bulkLoadOnce(smemDyn + size_t(st) * NBUF * sliceBytes, in + d.inPos * E, inBytes, &sh.fullIn[st], once);
       }
       mbarArrive(&sh.fullIn[st]);
       if (++st == NST) {
