@@ -511,7 +511,7 @@ struct Shape {
 // shape with which every agent of the launch is resident at once (all
 // agents wait on each other). grouped: the kernel is the grouped ring.
 static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto, size_t bytes, int kdtype, int kop,
-                                 size_t kE, bool grouped, Shape* out, Choice* tuned = nullptr) {
+                                 size_t kE, bool grouped, Shape* out) {
   const int n = comm->nranks;
   const bool userAlgo = coll == kAllReduce && algo != vrcclAlgoAuto && !grouped;
   const bool userProto = proto != vrcclProtoAuto;
@@ -528,7 +528,6 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
   if (algo == vrcclAlgoOneShot) protoMask = 1u << kSimple;
   if (!algoMask || !protoMask) return vrcclInvalidUsage;
   Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, algoMask, protoMask);
-  if (tuned) *tuned = ch;
   const int A = ch.algo, P = ch.proto;
   int C = comm->forceChannels ? comm->forceChannels
         : comm->envChannels   ? comm->envChannels
@@ -634,8 +633,7 @@ static unsigned long long stepBound(int n, unsigned long long elems, int C, int 
 
 static vrcclResult_t cooperativeLaunch(const void* fn, int blocks, int threads, size_t smem, void* arg,
                                        vrcclStream_t stream) {
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = smem;
