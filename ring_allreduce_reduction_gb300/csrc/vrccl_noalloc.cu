@@ -140,8 +140,7 @@ extern "C" vrcclResult_t vrcclAllReduceNoAlloc(const void* const* sendbufs, void
     ka.send[i] = sendbufs[i];
     ka.recv[i] = recvbufs[i];
   }
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(nranks * ka.nchannels));
   cfg.blockDim = dim3((unsigned)kNoAllocThreads);
   cfg.dynamicSmemBytes = kNoAllocSmem;
