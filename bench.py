@@ -11,7 +11,9 @@ Reported (one JSON line on rank 0):
   roofline  essential HBM bytes 2 n S per launch (read n inputs, write n
             outputs) / kernel time, against MEASURED_PEAKS.json's hbm_gbs
   e2e       the same metric with pinned host buffers: H2D of the inputs,
-            the AllReduce, D2H of the outputs, every step
+            the AllReduce, D2H of the outputs, every step; pipelined (the
+            buffers in 8 pieces, upload / AllReduce / download overlapping
+            on three streams), with the serial form beside it
   cpu_baseline  the CPU oracle replaying the same schedule on a bounded
             sample of the workload, on the host cores
 `--impl reference` times that oracle alone (the reference arm).
@@ -516,7 +518,61 @@ def main() -> int:
         e2e_ms = max_over_ranks(e2e_ms, "cuda")
         e2e = {"value": round(busbw_gbs(S, n, e2e_ms / 1e3, coll) * world, 3), "unit": "GB/s",
                "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
-               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": round(e2e_ms, 3)}
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": round(e2e_ms, 3),
+               "form": "serial: upload, AllReduce, download on one stream"}
+        del host_in, host_out
+        if coll == "allreduce" and count % 8 == 0:
+            # The same step as a user would pipeline it: the buffers in 8
+            # pieces, piece k+1's upload, piece k's AllReduce and piece
+            # k-1's download overlapping on three streams (the two copy
+            # directions run on separate copy engines).
+            K, pc = 8, count // 8
+            hin = torch.from_numpy(x).reshape(n, K, pc).permute(1, 0, 2).contiguous().pin_memory()  # [K, n, pc]
+            hout = torch.empty(hin.shape, dtype=hin.dtype).pin_memory()
+            dsend = torch.empty(hin.shape, dtype=hin.dtype, device="cuda")
+            drecv = torch.empty_like(dsend)
+            s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+            ev_in = [torch.cuda.Event() for _ in range(K)]
+            ev_red = [torch.cuda.Event() for _ in range(K)]
+            ev_out = [torch.cuda.Event() for _ in range(K)]
+            for k in range(K):  # events start completed
+                ev_red[k].record(stream)
+                ev_out[k].record(stream)
+
+            def pipe_step():
+                for k in range(K):
+                    s_in.wait_event(ev_red[k])  # the previous step's AllReduce of piece k read dsend[k]
+                    with torch.cuda.stream(s_in):
+                        dsend[k].copy_(hin[k], non_blocking=True)
+                    ev_in[k].record(s_in)
+                    stream.wait_event(ev_in[k])
+                    stream.wait_event(ev_out[k])  # the previous step's download of drecv[k]
+                    v.vrcclAllReduce([dsend[k, r] for r in range(n)], [drecv[k, r] for r in range(n)], pc, dtype,
+                                     W["op"], W["algo"], W["proto"], comm, stream)
+                    ev_red[k].record(stream)
+                    s_out.wait_event(ev_red[k])
+                    with torch.cuda.stream(s_out):
+                        hout[k].copy_(drecv[k], non_blocking=True)
+                    ev_out[k].record(s_out)
+
+            pipe_step()
+            torch.cuda.synchronize()
+            p0 = torch.cuda.Event(enable_timing=True)
+            p1 = torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            for _ in range(args.e2e_steps):
+                pipe_step()
+            stream.wait_event(ev_out[K - 1])
+            p1.record(stream)
+            torch.cuda.synchronize()
+            pipe_ms = max_over_ranks(p0.elapsed_time(p1) / args.e2e_steps, "cuda")
+            ok = np.array_equal(hout[K - 1, 0].numpy().view(np.uint32)[:4], hout[K - 1, 1].numpy().view(np.uint32)[:4])
+            serial = e2e
+            e2e = {"value": round(busbw_gbs(S, n, pipe_ms / 1e3, coll) * world, 3), "unit": "GB/s",
+                   "h2d_bytes_per_step": hin.numel() * hin.element_size(),
+                   "d2h_bytes_per_step": hout.numel() * hout.element_size(), "ms_per_step": round(pipe_ms, 3),
+                   "form": f"pipelined: {K} pieces of {pc} elements per rank, upload / AllReduce / download on "
+                           f"three streams", "ranks_agree": bool(ok), "serial": serial}
 
     # ---- the one-shot bound on the same buffers and schedule: every input
     # read once, every output written once, the ring's association order
