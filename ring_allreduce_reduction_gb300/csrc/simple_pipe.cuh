@@ -89,7 +89,18 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
   extern __shared__ __align__(128) char smemDyn[];
   __shared__ PipeShared sh;
   const DevComm& c = a.comm;
-  const int NST = a.stages;
+  // Buffers of one stage: the ring's input and received slot; for a tree
+  // agent those its role uses (its input if it reads it, one slot per
+  // in-edge). The block's dynamic shared memory, a.stages stages of NBUF
+  // slices, is cut into as many of this agent's stages as fit (at most
+  // kMaxStages), so down agents and leaves get deeper pipelines than the
+  // two-child agents the launch was sized for.
+  int inBuf = 1, nbuf = NBUF;
+  if constexpr (TREE) {
+    inBuf = (it.flags & F_IN) ? 1 : 0;
+    nbuf = max(1, inBuf + ag.nrecv);
+  }
+  const int NST = TREE ? min(kMaxStages, a.stages * NBUF / nbuf) : a.stages;
   const size_t sliceBytes = size_t(a.sliceElems) * E;
   const int W = (blockDim.x >> 5) - 3;  // consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,7 +148,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
       if (inBytes) {
         lastUse[st] = ph;
         mbarExpectTx(&sh.fullIn[st], inBytes);
-        bulkLoadOnce(smemDyn + size_t(st) * NBUF * sliceBytes, in + d.inPos * E, inBytes, &sh.fullIn[st], once);
+        bulkLoadOnce(smemDyn + size_t(st) * nbuf * sliceBytes, in + d.inPos * E, inBytes, &sh.fullIn[st], once);
       }
       mbarArrive(&sh.fullIn[st]);
       if (++st == NST) {
@@ -178,7 +189,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
         }
       }
       if (ok && (d.flags & F_RECV)) {
-        char* buf = smemDyn + size_t(st) * NBUF * sliceBytes;
+        char* buf = smemDyn + size_t(st) * nbuf * sliceBytes;
         for (int i = 0; i < ag.nrecv && ok; ++i) {
           const unsigned long long before = tailSeen[i];
           ok = flagAtLeast(c, ag, &c.ctrl[kSimple][ag.re[i]].tail, ag.rstep[i] + 1, tailSeen[i], 0);
@@ -186,7 +197,8 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
           if (tailSeen[i] != before) fenceProxyAsync();
           lastUse[st] = ph;
           mbarExpectTx(&sh.fullFifo[st], rvBytes);
-          bulkLoad(buf + size_t(1 + i) * sliceBytes, ag.slot(c, ag.re[i], ag.rstep[i]), rvBytes, &sh.fullFifo[st]);
+          bulkLoad(buf + size_t(inBuf + i) * sliceBytes, ag.slot(c, ag.re[i], ag.rstep[i]), rvBytes,
+                   &sh.fullFifo[st]);
         }
       }
       if (DIRECT && ok && (d.flags & F_DRECV) && (d.flags & F_DSEND)) {
@@ -200,7 +212,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
           if (dtailSeen != before) fenceProxyAsync();
           lastUse[st] = ph;
           mbarExpectTx(&sh.fullFifo[st], dBytes);
-          bulkLoad(smemDyn + size_t(st) * NBUF * sliceBytes + sliceBytes, out + d.outPos * E, dBytes,
+          bulkLoad(smemDyn + size_t(st) * nbuf * sliceBytes + size_t(inBuf) * sliceBytes, out + d.outPos * E, dBytes,
                    &sh.fullFifo[st]);
         }
       }
@@ -285,10 +297,10 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
     if (!pipeWait(c, ag, &sh, &sh.fullIn[st], ph)) return;
     if (!pipeWait(c, ag, &sh, &sh.fullFifo[st], ph)) return;
     if (*reinterpret_cast<volatile int*>(&sh.abort)) return;
-    const char* buf = smemDyn + size_t(st) * NBUF * sliceBytes;
+    const char* buf = smemDyn + size_t(st) * nbuf * sliceBytes;
     const char* sIn = buf;
-    const char* sR0 = buf + sliceBytes;
-    const char* sR1 = buf + 2 * sliceBytes;
+    const char* sR0 = buf + size_t(inBuf) * sliceBytes;
+    const char* sR1 = sR0 + sliceBytes;
     const bool rv = (d.flags & F_RECV) && ag.nrecv > 0;
     const bool drv = DIRECT && (d.flags & F_DRECV) && (d.flags & F_DSEND);  // staged from own recv buffer
     const int rf = d.flags | (drv ? F_RECV : 0);  // the reduction sees a received value
