@@ -4,22 +4,26 @@ Test infrastructure only. Every rank's output must be the elementwise op
 over all n inputs; the example program of [Deep Dive §1.3] checks exactly
 this (first element of every recv buffer = 0 + 1 + ... + (n-1)).
 
-* int32: sum and prod modulo 2^32, max/min, avg = wrapped sum divided by n
-  with truncation toward zero. These are exact and order-free, so any
-  schedule must match them bit for bit.
-* floating types: the float64 value of the op over the dtype-exact inputs
+* integer types (int8, uint8, int32, int64): sum and prod modulo 2^bits,
+  max/min (signed, unsigned for uint8), avg = wrapped sum divided by n with
+  truncation toward zero. These are exact and order-free, so any schedule
+  must match them bit for bit.
+* floating types: the exact value of the op over the dtype-exact inputs
   (pre-scaled by ``1/n`` and rounded to the dtype for avg, the same
-  operands the schedule adds). Bounds, per element, with ``u``-scale
-  tolerances of fp32 1e-5, bf16 (n+1) 2^-8, fp16 (n+1) 2^-11:
-  sum/avg ``|y - s64| <= tol * sum_i |x_i|`` (the recursive-summation
-  bound, safe under cancellation); prod ``|y - p64| <= tol * |p64|``;
-  max/min exact.
+  operands the schedule adds), computed in float64 for the 2- and 4-byte
+  types and in extended precision (numpy longdouble, at least 64 mantissa
+  bits) for float64. Bounds, per element, with ``u``-scale tolerances of
+  fp32 1e-5, bf16 (n+1) 2^-8, fp16 (n+1) 2^-11 and fp64 (n+1) 2^-53:
+  sum/avg ``|y - s| <= tol * sum_i |x_i|`` (the recursive-summation bound,
+  safe under cancellation); prod ``|y - p| <= tol * |p|``; max/min exact.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from . import numerics as nm
+
+_BITS = {"int8": 8, "uint8": 8, "int32": 32, "int64": 64}
 
 
 def tolerance(dtype: str, n: int) -> float:
@@ -29,42 +33,61 @@ def tolerance(dtype: str, n: int) -> float:
         return (n + 1) * 2.0 ** -8
     if dtype == "float16":
         return (n + 1) * 2.0 ** -11
+    if dtype == "float64":
+        return (n + 1) * 2.0 ** -53
     return 0.0
 
 
+def _wide(dtype: str):
+    return np.longdouble if dtype == "float64" else np.float64
+
+
 def operands(inputs: np.ndarray, op: str, dtype: str) -> np.ndarray:
-    """The per-rank operands as float64 (floats) or int64 (int32)."""
+    """The per-rank operands: exact integers (int64, or uint64 for the
+    64-bit wrap) for integer types; exact reals in float64 (longdouble for
+    float64) for floating types."""
     n = inputs.shape[0]
-    if dtype == "int32":
+    if dtype in nm.INT_TYPES:
         return np.asarray(inputs, dtype=np.int64)
     pre = np.stack([nm.prescale(inputs[r], op, dtype, n) for r in range(n)]) if n else inputs
+    if dtype == "float64":
+        return np.asarray(pre, dtype=np.float64).astype(np.longdouble)
     return nm.to_f32(pre, dtype).astype(np.float64)
 
 
 def exact(inputs: np.ndarray, op: str, dtype: str) -> np.ndarray:
-    """The closed form: float64 for floats, exact wrapped int32 for int32."""
+    """The closed form: exact wrapped integers for integer types, float64
+    (longdouble for float64) for floating types."""
     n = inputs.shape[0]
     x = operands(inputs, op, dtype)
-    if dtype == "int32":
-        m = np.uint64(1 << 32)
-        u = (x % (1 << 32)).astype(np.uint64)
+    if dtype in nm.INT_TYPES:
+        st = nm.INT_TYPES[dtype][0]
+        bits = _BITS[dtype]
+        if op == "max":
+            return x.max(axis=0).astype(st)
+        if op == "min":
+            return x.min(axis=0).astype(st)
+        u = x.view(np.uint64) if bits == 64 else (x % (1 << bits)).astype(np.uint64)
         if op in ("sum", "avg"):
-            acc = u.sum(axis=0, dtype=np.uint64) % m
+            acc = u.sum(axis=0, dtype=np.uint64)  # wraps modulo 2^64
         elif op == "prod":
             acc = np.ones(x.shape[1], dtype=np.uint64)
             for r in range(n):
-                acc = (acc * u[r]) % m  # both factors < 2^32: the product fits 64 bits
-        elif op == "max":
-            return x.max(axis=0).astype(np.int32)
-        elif op == "min":
-            return x.min(axis=0).astype(np.int32)
+                acc = acc * u[r]  # wraps modulo 2^64; the low `bits` bits are the product modulo 2^bits
         else:
             raise ValueError(op)
-        s = acc.astype(np.int64)
-        s = np.where(s >= (1 << 31), s - (1 << 32), s)
+        if bits < 64:
+            acc = acc % np.uint64(1 << bits)
+        signed = dtype != "uint8"
+        if bits == 64:
+            s = acc.view(np.int64)
+        else:
+            s = acc.astype(np.int64)
+            if signed:
+                s = np.where(s >= (1 << (bits - 1)), s - (1 << bits), s)
         if op == "avg":
-            s = (np.abs(s) // n) * np.sign(s)
-        return s.astype(np.int32)
+            s = nm.trunc_div(s, n) if signed else s // n
+        return s.astype(st)
     if op in ("sum", "avg"):
         return x.sum(axis=0)
     if op == "prod":
@@ -91,10 +114,13 @@ def bound(inputs: np.ndarray, op: str, dtype: str) -> np.ndarray:
 def check(result: np.ndarray, inputs: np.ndarray, op: str, dtype: str) -> tuple[bool, float]:
     """(within bounds?, worst excess ratio) of a ``[count]`` result row."""
     ref = exact(inputs, op, dtype)
-    if dtype == "int32":
-        ok = np.array_equal(np.asarray(result, dtype=np.int32), ref)
+    if dtype in nm.INT_TYPES:
+        ok = np.array_equal(np.asarray(result, dtype=nm.INT_TYPES[dtype][0]), ref)
         return ok, 0.0 if ok else float("inf")
-    y = nm.to_f32(result, dtype).astype(np.float64)
+    if dtype == "float64":
+        y = np.asarray(result, dtype=np.float64).astype(np.longdouble)
+    else:
+        y = nm.to_f32(result, dtype).astype(np.float64)
     err = np.abs(y - ref)
     b = bound(inputs, op, dtype)
     if op in ("max", "min"):

@@ -1,24 +1,28 @@
 """Element arithmetic of the oracle (test infrastructure only).
 
 Storage forms: int32 -> np.int32, float32 -> np.float32, float16 ->
-np.float16, bfloat16 -> np.uint16 holding the bf16 bit pattern.
+np.float16, bfloat16 -> np.uint16 holding the bf16 bit pattern, int8 ->
+np.int8, uint8 -> np.uint8, int64 -> np.int64, float64 -> np.float64.
 
-One reduction step ``combine(op, a, b)`` is, for floating types, the op in
-IEEE binary32 with round-to-nearest-even, then one rounding to the storage
-type (round-to-nearest-even). The pages leave the intermediate precision
-open: NCCL's FIFOs carry the user's dtype, so every hop of the ring stores
-(and therefore rounds to) that dtype [Architecture §7.2, the FIFO carries
-user data; Deep Dive §2.4]. For int32, sum and prod wrap modulo 2^32; max
-and min compare as signed.
+One reduction step ``combine(op, a, b)`` is, for the 2- and 4-byte floating
+types, the op in IEEE binary32 with round-to-nearest-even, then one
+rounding to the storage type (round-to-nearest-even); for float64 the op in
+binary64 (round-to-nearest-even). The pages leave the intermediate
+precision open: NCCL's FIFOs carry the user's dtype, so every hop of the
+ring stores (and therefore rounds to) that dtype [Architecture §7.2, the
+FIFO carries user data; Deep Dive §2.4]. Integer types: sum and prod wrap
+modulo 2^bits; max and min compare as signed (int8, int32, int64) or
+unsigned (uint8).
 
 Operand order: ``a`` is the running value (what arrived from the previous
 rank in the ring, or the node's own accumulator in the tree) and ``b`` the
 other operand. ``max(a, b) = b if b > a else a`` and ``min(a, b) = b if
 b < a else a``, so a tie (including +0 against -0) keeps ``a``.
 
-avg is not on the pages: for floating types every input is multiplied once
-by ``s = 1.0f / n`` (binary32, RNE) and rounded to the storage type before
-it enters the sum; for int32 the wrapped sum is divided by n with
+avg is not on the pages: for the 2- and 4-byte floating types every input
+is multiplied once by ``s = 1.0f / n`` (binary32, RNE) and rounded to the
+storage type before it enters the sum; for float64 by ``1.0 / n`` in
+binary64. For the integer types the wrapped sum is divided by n with
 truncation toward zero once, where the ring finishes a chunk (the post-op
 of the last reduce-scatter step, [Architecture §9.4]).
 """
@@ -27,7 +31,10 @@ from __future__ import annotations
 import numpy as np
 
 OPS = ("sum", "prod", "max", "min", "avg")
-FLOAT_TYPES = ("float32", "float16", "bfloat16")
+FLOAT_TYPES = ("float32", "float16", "bfloat16", "float64")
+# integer types: (storage type, unsigned type of the same width)
+INT_TYPES = {"int32": (np.int32, np.uint32), "int8": (np.int8, np.uint8), "uint8": (np.uint8, np.uint8),
+             "int64": (np.int64, np.uint64)}
 
 
 def to_f32(x: np.ndarray, dtype: str) -> np.ndarray:
@@ -77,19 +84,33 @@ def combine(op: str, a: np.ndarray, b: np.ndarray, dtype: str) -> np.ndarray:
     """One reduction step ``op(a, b)``; ``a`` is the running value."""
     if op == "avg":
         op = "sum"  # the pre-scale / post-op are applied outside
-    if dtype == "int32":
-        ua = np.asarray(a, dtype=np.int32).view(np.uint32)
-        ub = np.asarray(b, dtype=np.int32).view(np.uint32)
+    if dtype in INT_TYPES:
+        st, ut = INT_TYPES[dtype]
+        shape = np.broadcast_shapes(np.shape(a), np.shape(b))
+        ua = np.atleast_1d(np.asarray(a, dtype=st)).view(ut)
+        ub = np.atleast_1d(np.asarray(b, dtype=st)).view(ut)
         if op == "sum":
-            return (ua + ub).view(np.int32)
+            return (ua + ub).view(st).reshape(shape)  # unsigned arrays wrap modulo 2^bits
         if op == "prod":
-            return (ua * ub).view(np.int32)
-        a = np.asarray(a, dtype=np.int32)
-        b = np.asarray(b, dtype=np.int32)
+            return (ua * ub).view(st).reshape(shape)
+        a = np.asarray(a, dtype=st)
+        b = np.asarray(b, dtype=st)
         if op == "max":
             return np.where(b > a, b, a)
         if op == "min":
             return np.where(b < a, b, a)
+        raise ValueError(op)
+    if dtype == "float64":
+        fa = np.asarray(a, dtype=np.float64)
+        fb = np.asarray(b, dtype=np.float64)
+        if op == "sum":
+            return fa + fb
+        if op == "prod":
+            return fa * fb
+        if op == "max":
+            return np.where(fb > fa, fb, fa)
+        if op == "min":
+            return np.where(fb < fa, fb, fa)
         raise ValueError(op)
     fa = to_f32(a, dtype)
     fb = to_f32(b, dtype)
@@ -112,17 +133,32 @@ def avg_scale(n: int) -> np.float32:
 def prescale(x: np.ndarray, op: str, dtype: str, n: int) -> np.ndarray:
     """The value a rank feeds into the reduction for its own input x.
 
-    Identity except for floating avg, where it is ``rnd(float(x) * (1/n))``.
+    Identity except for floating avg, where it is ``rnd(float(x) * (1/n))``
+    (binary32 scale and product for the 2- and 4-byte types, binary64 for
+    float64).
     """
-    if op != "avg" or dtype == "int32":
+    if op != "avg" or dtype in INT_TYPES:
         return np.asarray(x)
+    if dtype == "float64":
+        return np.asarray(x, dtype=np.float64) * (np.float64(1.0) / np.float64(n))
     return from_f32(to_f32(x, dtype) * avg_scale(n), dtype)
 
 
-def postop(y: np.ndarray, op: str, dtype: str, n: int) -> np.ndarray:
-    """Applied once to a finished chunk: int32 avg divides by n, truncating."""
-    if op != "avg" or dtype != "int32":
-        return y
+def trunc_div(y: np.ndarray, n: int) -> np.ndarray:
+    """Integer division truncating toward zero, without overflow for any
+    64-bit y (floor quotient, plus one where a negative y left a
+    remainder)."""
     y64 = np.asarray(y, dtype=np.int64)
-    q = (np.abs(y64) // n) * np.sign(y64)
-    return q.astype(np.int32)
+    q = y64 // n
+    return q + ((y64 < 0) & (y64 % n != 0)).astype(np.int64)
+
+
+def postop(y: np.ndarray, op: str, dtype: str, n: int) -> np.ndarray:
+    """Applied once to a finished chunk: integer avg divides by n,
+    truncating toward zero."""
+    if op != "avg" or dtype not in INT_TYPES:
+        return y
+    st = INT_TYPES[dtype][0]
+    if dtype == "uint8":
+        return (np.asarray(y, dtype=np.uint8).astype(np.int64) // n).astype(np.uint8)
+    return trunc_div(np.asarray(y, dtype=st), n).astype(st)

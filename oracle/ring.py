@@ -41,7 +41,8 @@ import numpy as np
 from . import numerics as nm
 from .schedule import align_up, ceil_div, channel_ranges, ring_loops
 
-ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2, "int8": 1, "uint8": 1, "int64": 8,
+             "float64": 8}
 
 
 def ring_machine(local, combine_fn, post_fn, count: int, nchannels: int, chunk_elems: int,

@@ -11,7 +11,7 @@ Readings where the pages are silent:
 * order inside a node: the node's own (pre-scaled) value is the running
   value, then the value from child ``down[0]``, then from ``down[1]``:
   ``v = op(op(x_r, v_down0), v_down1)``;
-* the int32 avg post-op is applied once, at the root.
+* the integer avg post-op is applied once, at the root.
 
 The result depends on the tree and this order only, not on how the
 channel's range is cut into chunks, so no chunk size enters here.
@@ -23,7 +23,8 @@ import numpy as np
 from . import numerics as nm
 from .schedule import channel_ranges, channel_tree, get_dtree
 
-ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2, "int8": 1, "uint8": 1, "int64": 8,
+             "float64": 8}
 
 
 def tree_links(nranks: int, which: int) -> list[tuple[int, int, int]]:

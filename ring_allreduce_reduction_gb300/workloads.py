@@ -17,7 +17,14 @@ float32    ``np.float32``      the value
 float16    ``np.float16``      the value
 bfloat16   ``np.uint16``       the bf16 bit pattern (sign, 8-bit
                                exponent, 7-bit mantissa)
+int8       ``np.int8``         the value
+uint8      ``np.uint8``        the value
+int64      ``np.int64``        the value
+float64    ``np.float64``      the value
 =========  ==================  =========================================
+
+Real-valued draws are binary32 for the 2- and 4-byte floating types and
+binary64 for float64.
 
 bf16 values are made by keeping the upper 16 bits of a float32 draw
 (truncation toward zero). That is a recipe for drawing inputs, not a
@@ -27,10 +34,13 @@ from __future__ import annotations
 
 import numpy as np
 
-DTYPES = ("int32", "float32", "bfloat16", "float16")
-ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+DTYPES = ("int32", "float32", "bfloat16", "float16", "int8", "uint8", "int64", "float64")
+ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2, "int8": 1, "uint8": 1, "int64": 8,
+             "float64": 8}
 STORAGE = {"int32": np.int32, "float32": np.float32, "bfloat16": np.uint16,
-           "float16": np.float16}
+           "float16": np.float16, "int8": np.int8, "uint8": np.uint8, "int64": np.int64,
+           "float64": np.float64}
+INT_TYPES = ("int32", "int8", "uint8", "int64")
 
 
 def rank_generators(n: int, seed: int = 0) -> list[np.random.Generator]:
@@ -43,8 +53,10 @@ def _bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
 
 
 def _store(vals: np.ndarray, dtype: str) -> np.ndarray:
-    if dtype == "int32":
-        return vals.astype(np.int32)
+    if dtype in INT_TYPES:
+        return vals.astype(STORAGE[dtype])
+    if dtype == "float64":
+        return vals.astype(np.float64)
     if dtype == "float32":
         return vals.astype(np.float32)
     if dtype == "float16":
@@ -78,14 +90,20 @@ def make_inputs(n: int, count: int, dtype: str, dist: str = "uniform", seed: int
             v = g.integers(int(lo), int(hi), size=count, endpoint=True, dtype=np.int64)
             out[r] = _store(v, dtype)
         elif dist == "uniform":
-            v = g.random(count, dtype=np.float32) * np.float32(hi - lo) + np.float32(lo)
-            if dtype == "int32":
-                raise ValueError("use int_uniform for int32")
+            if dtype in INT_TYPES:
+                raise ValueError(f"use int_uniform for {dtype}")
+            if dtype == "float64":
+                v = g.random(count) * (hi - lo) + lo
+            else:
+                v = g.random(count, dtype=np.float32) * np.float32(hi - lo) + np.float32(lo)
             out[r] = _store(v, dtype)
         elif dist == "normal":
-            v = g.standard_normal(count, dtype=np.float32) * np.float32(std)
-            if dtype == "int32":
-                raise ValueError("use int_uniform for int32")
+            if dtype in INT_TYPES:
+                raise ValueError(f"use int_uniform for {dtype}")
+            if dtype == "float64":
+                v = g.standard_normal(count) * std
+            else:
+                v = g.standard_normal(count, dtype=np.float32) * np.float32(std)
             out[r] = _store(v, dtype)
         else:
             raise ValueError(f"unknown dist {dist!r}")

@@ -291,13 +291,18 @@ def test_allreduce_example_first_element():
 OPS = ["sum", "prod", "max", "min", "avg"]
 
 
-@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16", "float16"])
+ALL_DTYPES = ["int32", "float32", "bfloat16", "float16", "int8", "uint8", "int64", "float64"]
+INT_RANGE = {"int32": (-2**20, 2**20), "int8": (-128, 127), "uint8": (0, 255), "int64": (-2**62, 2**62)}
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("n", [1, 2, 3, 5, 8])
 def test_ring_matches_closed_form(dtype, op, n):
     count = 1000 + n
-    if dtype == "int32":
-        x = make_inputs(n, count, dtype, "int_uniform", seed=7, lo=-2**20, hi=2**20)
+    if dtype in INT_RANGE:
+        lo, hi = INT_RANGE[dtype]
+        x = make_inputs(n, count, dtype, "int_uniform", seed=7, lo=lo, hi=hi)
     elif op == "prod":
         x = make_inputs(n, count, dtype, "uniform", seed=7, lo=0.5, hi=2.0)
     else:
@@ -367,13 +372,14 @@ def test_tree_symbolic_association(n, nch):
                 assert all(outs[r][i] == want for i in range(lo, hi))
 
 
-@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16", "float16"])
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
 @pytest.mark.parametrize("op", OPS)
 @pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
 def test_tree_matches_closed_form(dtype, op, n):
     count = 777
-    if dtype == "int32":
-        x = make_inputs(n, count, dtype, "int_uniform", seed=9, lo=-2**20, hi=2**20)
+    if dtype in INT_RANGE:
+        lo, hi = INT_RANGE[dtype]
+        x = make_inputs(n, count, dtype, "int_uniform", seed=9, lo=lo, hi=hi)
     elif op == "prod":
         x = make_inputs(n, count, dtype, "uniform", seed=9, lo=0.5, hi=2.0)
     else:
