@@ -95,12 +95,22 @@ typedef enum {
   vrcclNumResults = 7
 } vrcclResult_t;
 
+/* Element types [Deep Dive §1.3, ncclDataType_t]. Integer sum and prod
+ * wrap modulo 2^bits, max and min compare signed (unsigned for uint8), avg
+ * is the wrapped sum divided by n, truncating toward zero. bf16 / fp16 /
+ * fp32 combine in binary32 and round to the type at every hop; fp64
+ * combines in binary64; avg pre-scales each input by 1/n (binary32 for
+ * the 2- and 4-byte types, binary64 for fp64). */
 typedef enum {
   vrcclInt32 = 0,
   vrcclFloat32 = 1,
   vrcclBfloat16 = 2,
   vrcclFloat16 = 3,
-  vrcclNumTypes = 4
+  vrcclInt8 = 4,
+  vrcclUint8 = 5,
+  vrcclInt64 = 6,
+  vrcclFloat64 = 7,
+  vrcclNumTypes = 8
 } vrcclDataType_t;
 
 typedef enum {

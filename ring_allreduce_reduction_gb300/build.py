@@ -22,7 +22,8 @@ LIB = os.path.join(PKG, "libvrccl.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}",
          "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
-SOURCES = ["kernels_simple.cu", "kernels_ll.cu", "kernels_ll128.cu", "kernels_ll128w.cu", "kernels_oneshot.cu", "kernels_group_simple.cu",
+SOURCES = ["kernels_simple.cu", "kernels_simple_x.cu", "kernels_ll.cu", "kernels_ll128.cu", "kernels_ll128w.cu",
+           "kernels_ll128w_x.cu", "kernels_oneshot.cu", "kernels_group_simple.cu",
            "kernels_group_ll.cu", "kernels_group_ll128.cu", "vrccl.cu", "vrccl_noalloc.cu", "tuner.cc", "parse.cc",
            "model.cc"]
 

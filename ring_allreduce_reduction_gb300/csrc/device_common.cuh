@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "vrccl_internal.h"
 
@@ -217,6 +218,18 @@ template <> struct Ty<vrcclInt32> {
   using S = int32_t;
   static constexpr bool kFloat = false;
 };
+template <> struct Ty<vrcclInt8> {
+  using S = int8_t;
+  static constexpr bool kFloat = false;
+};
+template <> struct Ty<vrcclUint8> {
+  using S = uint8_t;
+  static constexpr bool kFloat = false;
+};
+template <> struct Ty<vrcclInt64> {
+  using S = long long;
+  static constexpr bool kFloat = false;
+};
 template <> struct Ty<vrcclFloat32> {
   using S = float;
   static constexpr bool kFloat = true;
@@ -237,15 +250,29 @@ template <> struct Ty<vrcclFloat16> {
   __device__ static __forceinline__ float toF(unsigned short x) { return __half2float(__ushort_as_half(x)); }
   __device__ static __forceinline__ unsigned short fromF(float x) { return __half_as_ushort(__float2half_rn(x)); }
 };
+// float64 computes in binary64 itself (no widening type).
+template <> struct Ty<vrcclFloat64> {
+  using S = double;
+  static constexpr bool kFloat = true;
+};
 
-// One reduction step op(a, b); a is the running value. Floating types: the
-// op in binary32 without contraction, then one rounding to the type; max
-// and min keep `a` on a tie. int32 sum/prod wrap.
+// One reduction step op(a, b); a is the running value. 2- and 4-byte
+// floating types: the op in binary32 without contraction, then one rounding
+// to the type; float64: the op in binary64. max and min keep `a` on a tie.
+// Integer sum/prod wrap modulo 2^bits (computed in the unsigned type of the
+// same width); max/min compare in the type (uint8 unsigned).
 template <int DT, int OP>
 __device__ __forceinline__ typename Ty<DT>::S combine(typename Ty<DT>::S a, typename Ty<DT>::S b) {
+  using S = typename Ty<DT>::S;
   if constexpr (!Ty<DT>::kFloat) {
-    if constexpr (OP == vrcclSum || OP == vrcclAvg) return int32_t(uint32_t(a) + uint32_t(b));
-    if constexpr (OP == vrcclProd) return int32_t(uint32_t(a) * uint32_t(b));
+    using U = std::make_unsigned_t<S>;
+    if constexpr (OP == vrcclSum || OP == vrcclAvg) return S(U(U(a) + U(b)));
+    if constexpr (OP == vrcclProd) return S(U(U(a) * U(b)));
+    if constexpr (OP == vrcclMax) return b > a ? b : a;
+    if constexpr (OP == vrcclMin) return b < a ? b : a;
+  } else if constexpr (DT == vrcclFloat64) {
+    if constexpr (OP == vrcclSum || OP == vrcclAvg) return __dadd_rn(a, b);
+    if constexpr (OP == vrcclProd) return __dmul_rn(a, b);
     if constexpr (OP == vrcclMax) return b > a ? b : a;
     if constexpr (OP == vrcclMin) return b < a ? b : a;
   } else {
@@ -257,28 +284,55 @@ __device__ __forceinline__ typename Ty<DT>::S combine(typename Ty<DT>::S a, type
   }
 }
 
-// What a rank feeds into the reduction for its own element (avg scale).
+// What a rank feeds into the reduction for its own element (avg scale):
+// the binary32 1/n for the 2- and 4-byte floating types, the binary64 1/n
+// for float64.
 template <int DT, int OP>
-__device__ __forceinline__ typename Ty<DT>::S prescale(typename Ty<DT>::S x, float scale) {
-  if constexpr (OP == vrcclAvg && Ty<DT>::kFloat) return Ty<DT>::fromF(__fmul_rn(Ty<DT>::toF(x), scale));
-  return x;
+__device__ __forceinline__ typename Ty<DT>::S prescale(typename Ty<DT>::S x, float scale, int n) {
+  if constexpr (OP == vrcclAvg && DT == vrcclFloat64) {
+    return __dmul_rn(x, 1.0 / double(n));
+  } else if constexpr (OP == vrcclAvg && Ty<DT>::kFloat) {
+    return Ty<DT>::fromF(__fmul_rn(Ty<DT>::toF(x), scale));
+  } else {
+    return x;
+  }
 }
 
-// Applied where a chunk becomes final: int32 avg divides, truncating.
+// Applied where a chunk becomes final: integer avg divides, truncating
+// toward zero (C++ integer division).
 template <int DT, int OP>
 __device__ __forceinline__ typename Ty<DT>::S postop(typename Ty<DT>::S x, int n) {
-  if constexpr (OP == vrcclAvg && !Ty<DT>::kFloat) return x / n;
+  using S = typename Ty<DT>::S;
+  if constexpr (OP == vrcclAvg && !Ty<DT>::kFloat) return S(x / n);
   return x;
 }
 
 // ------------------------------------------------------------ packed words
-// A 32-bit word holds one 4-byte element or two 2-byte elements (element 0
-// in the low half, as they sit in memory).
+// Data moves as 32-bit words. A word holds one 4-byte element, two 2-byte
+// elements or four 1-byte elements (element 0 in the low bits, as they sit
+// in memory); an 8-byte element spans two consecutive words (low word
+// first). The word-array forms below take NW words whose boundaries are
+// element boundaries.
 
 __device__ __forceinline__ int32_t fromWord(uint32_t w, int32_t*) { return int32_t(w); }
 __device__ __forceinline__ float fromWord(uint32_t w, float*) { return __uint_as_float(w); }
 __device__ __forceinline__ uint32_t toWord(int32_t x) { return uint32_t(x); }
 __device__ __forceinline__ uint32_t toWord(float x) { return __float_as_uint(x); }
+
+template <typename S>
+__device__ __forceinline__ S fromPair(uint32_t lo, uint32_t hi) {
+  const unsigned long long v = (unsigned long long)lo | ((unsigned long long)hi << 32);
+  S x;
+  memcpy(&x, &v, 8);
+  return x;
+}
+template <typename S>
+__device__ __forceinline__ void toPair(S x, uint32_t& lo, uint32_t& hi) {
+  unsigned long long v;
+  memcpy(&v, &x, 8);
+  lo = uint32_t(v);
+  hi = uint32_t(v >> 32);
+}
 
 // Two 2-byte sums in one instruction. For bf16 and fp16 the binary32 sum
 // of two values of the type is either exact or differs from the exact sum
@@ -296,28 +350,42 @@ __device__ __forceinline__ uint32_t addF16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// op on the elements of one word (not for 8-byte types).
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t combineWord(uint32_t a, uint32_t b) {
   using S = typename Ty<DT>::S;
+  static_assert(sizeof(S) <= 4, "8-byte elements span two words");
   if constexpr (sizeof(S) == 4) {
     return toWord(combine<DT, OP>(fromWord(a, (S*)nullptr), fromWord(b, (S*)nullptr)));
   } else if constexpr ((OP == vrcclSum || OP == vrcclAvg) && DT == vrcclBfloat16) {
     return addBf16x2(a, b);
   } else if constexpr ((OP == vrcclSum || OP == vrcclAvg) && DT == vrcclFloat16) {
     return addF16x2(a, b);
-  } else {
+  } else if constexpr (sizeof(S) == 2) {
     uint32_t lo = combine<DT, OP>(S(a & 0xffffu), S(b & 0xffffu));
     uint32_t hi = combine<DT, OP>(S(a >> 16), S(b >> 16));
     return lo | (hi << 16);
+  } else if constexpr (OP == vrcclSum || OP == vrcclAvg) {
+    return __vadd4(a, b);  // four byte sums modulo 2^8, no carry between bytes
+  } else if constexpr (OP == vrcclMax) {
+    return DT == vrcclInt8 ? __vmaxs4(a, b) : __vmaxu4(a, b);
+  } else if constexpr (OP == vrcclMin) {
+    return DT == vrcclInt8 ? __vmins4(a, b) : __vminu4(a, b);
+  } else {
+    uint32_t d = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d |= (((a >> (8 * i)) * (b >> (8 * i))) & 0xffu) << (8 * i);
+    return d;
   }
 }
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t prescaleWord(uint32_t a, float scale) {
   using S = typename Ty<DT>::S;
+  static_assert(sizeof(S) <= 4, "8-byte elements span two words");
   if constexpr (!(OP == vrcclAvg && Ty<DT>::kFloat)) {
     return a;
   } else if constexpr (sizeof(S) == 4) {
-    return toWord(prescale<DT, OP>(fromWord(a, (S*)nullptr), scale));
+    return toWord(prescale<DT, OP>(fromWord(a, (S*)nullptr), scale, 1));
   } else {
     // binary32 products, then both rounded (to nearest even) by one packed
     // conversion; the high half of the word is the second element.
@@ -333,8 +401,54 @@ __device__ __forceinline__ uint32_t prescaleWord(uint32_t a, float scale) {
 }
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t postopWord(uint32_t a, int n) {
-  if constexpr (OP == vrcclAvg && !Ty<DT>::kFloat) return uint32_t(int32_t(a) / n);
-  return a;
+  using S = typename Ty<DT>::S;
+  static_assert(sizeof(S) <= 4, "8-byte elements span two words");
+  if constexpr (!(OP == vrcclAvg && !Ty<DT>::kFloat)) {
+    return a;
+  } else if constexpr (sizeof(S) == 4) {
+    return uint32_t(int32_t(a) / n);
+  } else {
+    uint32_t d = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d |= (uint32_t(uint8_t(postop<DT, OP>(S(a >> (8 * i)), n)))) << (8 * i);
+    return d;
+  }
+}
+
+// The same three steps on NW words (whole elements).
+template <int DT, int OP, int NW>
+__device__ __forceinline__ void combineWords(uint32_t (&a)[NW], const uint32_t (&b)[NW]) {
+  using S = typename Ty<DT>::S;
+  if constexpr (sizeof(S) == 8) {
+#pragma unroll
+    for (int w = 0; w < NW; w += 2)
+      toPair(combine<DT, OP>(fromPair<S>(a[w], a[w + 1]), fromPair<S>(b[w], b[w + 1])), a[w], a[w + 1]);
+  } else {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) a[w] = combineWord<DT, OP>(a[w], b[w]);
+  }
+}
+template <int DT, int OP, int NW>
+__device__ __forceinline__ void prescaleWords(uint32_t (&a)[NW], float scale, int n) {
+  using S = typename Ty<DT>::S;
+  if constexpr (sizeof(S) == 8) {
+#pragma unroll
+    for (int w = 0; w < NW; w += 2) toPair(prescale<DT, OP>(fromPair<S>(a[w], a[w + 1]), scale, n), a[w], a[w + 1]);
+  } else {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) a[w] = prescaleWord<DT, OP>(a[w], scale);
+  }
+}
+template <int DT, int OP, int NW>
+__device__ __forceinline__ void postopWords(uint32_t (&a)[NW], int n) {
+  using S = typename Ty<DT>::S;
+  if constexpr (sizeof(S) == 8) {
+#pragma unroll
+    for (int w = 0; w < NW; w += 2) toPair(postop<DT, OP>(fromPair<S>(a[w], a[w + 1]), n), a[w], a[w + 1]);
+  } else {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) a[w] = postopWord<DT, OP>(a[w], n);
+  }
 }
 
 }  // namespace vrccl

@@ -128,23 +128,42 @@ __device__ __forceinline__ void reduceWords(uint32_t (&acc)[NW], const uint32_t 
                                             const uint32_t (&r1)[NW], int flags, int nrecv, float scale, int n) {
   const bool in = flags & F_IN;
   const bool rv = (flags & F_RECV) && nrecv > 0;
+  if constexpr (sizeof(typename Ty<DT>::S) == 8) {
+    // 8-byte elements: the same steps on word pairs
+    uint32_t own[NW], v[NW];
 #pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    uint32_t own = in ? prescaleWord<DT, OP>(x[w], scale) : 0u;
-    uint32_t v;
+    for (int w = 0; w < NW; ++w) own[w] = in ? x[w] : 0u;
+    if (in) prescaleWords<DT, OP, NW>(own, scale, n);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) v[w] = (TREE ? !in : rv) ? r0[w] : own[w];
     if constexpr (!TREE) {
-      v = rv ? (in ? combineWord<DT, OP>(r0[w], own) : r0[w]) : own;
+      if (rv && in) combineWords<DT, OP, NW>(v, own);
     } else {
-      if (in) {
-        v = own;
-        if (rv) v = combineWord<DT, OP>(v, r0[w]);
-        if (rv && nrecv > 1) v = combineWord<DT, OP>(v, r1[w]);
-      } else {
-        v = r0[w];
-      }
+      if (in && rv) combineWords<DT, OP, NW>(v, r0);
+      if (in && rv && nrecv > 1) combineWords<DT, OP, NW>(v, r1);
     }
-    if (flags & F_POST) v = postopWord<DT, OP>(v, n);
-    acc[w] = v;
+    if (flags & F_POST) postopWords<DT, OP, NW>(v, n);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) acc[w] = v[w];
+  } else {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      uint32_t own = in ? prescaleWord<DT, OP>(x[w], scale) : 0u;
+      uint32_t v;
+      if constexpr (!TREE) {
+        v = rv ? (in ? combineWord<DT, OP>(r0[w], own) : r0[w]) : own;
+      } else {
+        if (in) {
+          v = own;
+          if (rv) v = combineWord<DT, OP>(v, r0[w]);
+          if (rv && nrecv > 1) v = combineWord<DT, OP>(v, r1[w]);
+        } else {
+          v = r0[w];
+        }
+      }
+      if (flags & F_POST) v = postopWord<DT, OP>(v, n);
+      acc[w] = v;
+    }
   }
 }
 
@@ -156,7 +175,7 @@ __device__ __forceinline__ typename Ty<DT>::S reduceElem(typename Ty<DT>::S x, t
   using S = typename Ty<DT>::S;
   const bool in = flags & F_IN;
   const bool rv = (flags & F_RECV) && nrecv > 0;
-  S own = in ? prescale<DT, OP>(x, scale) : S(0);
+  S own = in ? prescale<DT, OP>(x, scale, n) : S(0);
   S v;
   if constexpr (!TREE) {
     v = rv ? (in ? combine<DT, OP>(r0, own) : r0) : own;
@@ -180,13 +199,7 @@ template <typename S>
 __device__ __forceinline__ uint2 loadUnit(const char* p, int validBytes) {
   if (validBytes >= 8) return ldStream8(p);
   uint32_t w[2] = {0u, 0u};
-  for (int e = 0; e < validBytes / int(sizeof(S)); ++e) {
-    S v = reinterpret_cast<const S*>(p)[e];
-    uint32_t bits = sizeof(S) == 4 ? *reinterpret_cast<const uint32_t*>(&v)
-                                   : uint32_t(*reinterpret_cast<const unsigned short*>(&v));
-    const int byte = e * int(sizeof(S));
-    w[byte / 4] |= bits << (8 * (byte % 4));
-  }
+  for (int b = 0; b < validBytes; ++b) w[b >> 2] |= uint32_t((unsigned char)p[b]) << (8 * (b & 3));
   return make_uint2(w[0], w[1]);
 }
 template <typename S>
@@ -196,15 +209,7 @@ __device__ __forceinline__ void storeUnit(char* p, uint2 v, int validBytes) {
     return;
   }
   const uint32_t w[2] = {v.x, v.y};
-  for (int e = 0; e < validBytes / int(sizeof(S)); ++e) {
-    const int byte = e * int(sizeof(S));
-    uint32_t bits = w[byte / 4] >> (8 * (byte % 4));
-    if constexpr (sizeof(S) == 4) {
-      reinterpret_cast<uint32_t*>(p)[e] = bits;
-    } else {
-      reinterpret_cast<unsigned short*>(p)[e] = (unsigned short)(bits & 0xffffu);
-    }
-  }
+  for (int b = 0; b < validBytes; ++b) p[b] = char((w[b >> 2] >> (8 * (b & 3))) & 0xffu);
 }
 
 // ---------------------------------------------------------------------- LL

@@ -85,7 +85,8 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) groupRingKernel(const 
   {(const void*)groupRingKernel<PROTO, DT, 0>, (const void*)groupRingKernel<PROTO, DT, 1>, \
    (const void*)groupRingKernel<PROTO, DT, 2>, (const void*)groupRingKernel<PROTO, DT, 3>, \
    (const void*)groupRingKernel<PROTO, DT, 4>}
-#define VRCCL_GROUP_TABLE(PROTO) \
-  {VRCCL_GROUP_ROW(PROTO, 0), VRCCL_GROUP_ROW(PROTO, 1), VRCCL_GROUP_ROW(PROTO, 2), VRCCL_GROUP_ROW(PROTO, 3)}
+#define VRCCL_GROUP_TABLE(PROTO)                                                                 \
+  {VRCCL_GROUP_ROW(PROTO, 0), VRCCL_GROUP_ROW(PROTO, 1), VRCCL_GROUP_ROW(PROTO, 2), VRCCL_GROUP_ROW(PROTO, 3), \
+   VRCCL_GROUP_ROW(PROTO, 4), VRCCL_GROUP_ROW(PROTO, 5), VRCCL_GROUP_ROW(PROTO, 6), VRCCL_GROUP_ROW(PROTO, 7)}
 
 }  // namespace vrccl

@@ -213,22 +213,19 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) treeKernel(const __gri
   }
 }
 
-// Explicit instantiation of every (dtype, op) for one protocol, and its
-// row of the kernel table.
-#define VRCCL_KERNEL_ROW(PROTO, ALGO_KERNEL)                                                        \
-  {                                                                                                 \
-    {(const void*)ALGO_KERNEL<PROTO, 0, 0>, (const void*)ALGO_KERNEL<PROTO, 0, 1>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 0, 2>, (const void*)ALGO_KERNEL<PROTO, 0, 3>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 0, 4>},                                                        \
-    {(const void*)ALGO_KERNEL<PROTO, 1, 0>, (const void*)ALGO_KERNEL<PROTO, 1, 1>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 1, 2>, (const void*)ALGO_KERNEL<PROTO, 1, 3>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 1, 4>},                                                        \
-    {(const void*)ALGO_KERNEL<PROTO, 2, 0>, (const void*)ALGO_KERNEL<PROTO, 2, 1>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 2, 2>, (const void*)ALGO_KERNEL<PROTO, 2, 3>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 2, 4>},                                                        \
-    {(const void*)ALGO_KERNEL<PROTO, 3, 0>, (const void*)ALGO_KERNEL<PROTO, 3, 1>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 3, 2>, (const void*)ALGO_KERNEL<PROTO, 3, 3>,                  \
-     (const void*)ALGO_KERNEL<PROTO, 3, 4>},                                                        \
-  }
+// Explicit instantiation of every op of element types D0 .. D0+3 (or of all
+// eight) for one protocol: rows of the kernel table.
+#define VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, DT)                                                   \
+  {(const void*)ALGO_KERNEL<PROTO, DT, 0>, (const void*)ALGO_KERNEL<PROTO, DT, 1>,                   \
+   (const void*)ALGO_KERNEL<PROTO, DT, 2>, (const void*)ALGO_KERNEL<PROTO, DT, 3>,                   \
+   (const void*)ALGO_KERNEL<PROTO, DT, 4>}
+#define VRCCL_KERNEL_ROWS4(PROTO, ALGO_KERNEL, D0)                                                    \
+  {VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, D0), VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, D0 + 1),     \
+   VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, D0 + 2), VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, D0 + 3)}
+#define VRCCL_KERNEL_ROWS8(PROTO, ALGO_KERNEL)                                                        \
+  {VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 0), VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 1),           \
+   VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 2), VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 3),           \
+   VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 4), VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 5),           \
+   VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 6), VRCCL_KERNEL_DT_ROW(PROTO, ALGO_KERNEL, 7)}
 
 }  // namespace vrccl

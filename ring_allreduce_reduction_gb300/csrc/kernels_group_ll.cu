@@ -3,6 +3,6 @@
 #include "group.cuh"
 
 namespace vrccl {
-extern const void* const kGroupLL[4][5];
-const void* const kGroupLL[4][5] = VRCCL_GROUP_TABLE(kLL);
+extern const void* const kGroupLL[vrcclNumTypes][5];
+const void* const kGroupLL[vrcclNumTypes][5] = VRCCL_GROUP_TABLE(kLL);
 }  // namespace vrccl

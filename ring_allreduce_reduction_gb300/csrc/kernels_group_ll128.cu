@@ -3,6 +3,6 @@
 #include "group.cuh"
 
 namespace vrccl {
-extern const void* const kGroupLL128[4][5];
-const void* const kGroupLL128[4][5] = VRCCL_GROUP_TABLE(kLL128);
+extern const void* const kGroupLL128[vrcclNumTypes][5];
+const void* const kGroupLL128[vrcclNumTypes][5] = VRCCL_GROUP_TABLE(kLL128);
 }  // namespace vrccl

@@ -3,6 +3,6 @@
 #include "group.cuh"
 
 namespace vrccl {
-extern const void* const kGroupSimple[4][5];
-const void* const kGroupSimple[4][5] = VRCCL_GROUP_TABLE(kSimple);
+extern const void* const kGroupSimple[vrcclNumTypes][5];
+const void* const kGroupSimple[vrcclNumTypes][5] = VRCCL_GROUP_TABLE(kSimple);
 }  // namespace vrccl

@@ -3,8 +3,8 @@
 #include "kernels.cuh"
 
 namespace vrccl {
-extern const void* const kRingLL[4][5];
-extern const void* const kTreeLL[4][5];
-const void* const kRingLL[4][5] = VRCCL_KERNEL_ROW(kLL, ringKernel);
-const void* const kTreeLL[4][5] = VRCCL_KERNEL_ROW(kLL, treeKernel);
+extern const void* const kRingLL[vrcclNumTypes][5];
+extern const void* const kTreeLL[vrcclNumTypes][5];
+const void* const kRingLL[vrcclNumTypes][5] = VRCCL_KERNEL_ROWS8(kLL, ringKernel);
+const void* const kTreeLL[vrcclNumTypes][5] = VRCCL_KERNEL_ROWS8(kLL, treeKernel);
 }  // namespace vrccl

@@ -3,8 +3,8 @@
 #include "kernels.cuh"
 
 namespace vrccl {
-extern const void* const kRingLL128[4][5];
-extern const void* const kTreeLL128[4][5];
-const void* const kRingLL128[4][5] = VRCCL_KERNEL_ROW(kLL128, ringKernel);
-const void* const kTreeLL128[4][5] = VRCCL_KERNEL_ROW(kLL128, treeKernel);
+extern const void* const kRingLL128[vrcclNumTypes][5];
+extern const void* const kTreeLL128[vrcclNumTypes][5];
+const void* const kRingLL128[vrcclNumTypes][5] = VRCCL_KERNEL_ROWS8(kLL128, ringKernel);
+const void* const kTreeLL128[vrcclNumTypes][5] = VRCCL_KERNEL_ROWS8(kLL128, treeKernel);
 }  // namespace vrccl

@@ -63,8 +63,8 @@ __global__ void __launch_bounds__(kOneShotThreads) oneShotKernel(const __grid_co
       if (e >= cp.end) cp = ringChunkOf(e, count, n, a.nchannels, K, V);
       int rk = cp.j + 1 == n ? 0 : cp.j + 1;
       uint4 v0 = ldStream16(reinterpret_cast<const char*>(a.send[rk]) + e * E);
-      uint32_t acc[4] = {prescaleWord<DT, OP>(v0.x, a.scale), prescaleWord<DT, OP>(v0.y, a.scale),
-                         prescaleWord<DT, OP>(v0.z, a.scale), prescaleWord<DT, OP>(v0.w, a.scale)};
+      uint32_t acc[4] = {v0.x, v0.y, v0.z, v0.w};
+      prescaleWords<DT, OP, 4>(acc, a.scale, n);
       int left = n - 1;
       while (left > 0) {
         const int g = left < G ? left : G;
@@ -80,17 +80,16 @@ __global__ void __launch_bounds__(kOneShotThreads) oneShotKernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < G; ++i) {
           if (i < g) {
-            acc[0] = combineWord<DT, OP>(acc[0], prescaleWord<DT, OP>(v[i].x, a.scale));
-            acc[1] = combineWord<DT, OP>(acc[1], prescaleWord<DT, OP>(v[i].y, a.scale));
-            acc[2] = combineWord<DT, OP>(acc[2], prescaleWord<DT, OP>(v[i].z, a.scale));
-            acc[3] = combineWord<DT, OP>(acc[3], prescaleWord<DT, OP>(v[i].w, a.scale));
+            uint32_t b[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            prescaleWords<DT, OP, 4>(b, a.scale, n);
+            combineWords<DT, OP, 4>(acc, b);
           }
         }
         rk = q;
         left -= g;
       }
-      const uint4 out = make_uint4(postopWord<DT, OP>(acc[0], n), postopWord<DT, OP>(acc[1], n),
-                                   postopWord<DT, OP>(acc[2], n), postopWord<DT, OP>(acc[3], n));
+      postopWords<DT, OP, 4>(acc, n);
+      const uint4 out = make_uint4(acc[0], acc[1], acc[2], acc[3]);
       for (int r = 0; r < n; ++r) stStream16(reinterpret_cast<char*>(a.recv[r]) + e * E, out);
     }
   }
@@ -101,10 +100,10 @@ __global__ void __launch_bounds__(kOneShotThreads) oneShotKernel(const __grid_co
     if (threadIdx.x < V && idx < count) {
       const int j = ringChunkOf(idx, count, n, a.nchannels, K, V).j;
       int rk = j + 1 == n ? 0 : j + 1;
-      S acc = prescale<DT, OP>(reinterpret_cast<const S*>(a.send[rk])[idx], a.scale);
+      S acc = prescale<DT, OP>(reinterpret_cast<const S*>(a.send[rk])[idx], a.scale, n);
       for (int i = 1; i < n; ++i) {
         rk = rk + 1 == n ? 0 : rk + 1;
-        acc = combine<DT, OP>(acc, prescale<DT, OP>(reinterpret_cast<const S*>(a.send[rk])[idx], a.scale));
+        acc = combine<DT, OP>(acc, prescale<DT, OP>(reinterpret_cast<const S*>(a.send[rk])[idx], a.scale, n));
       }
       acc = postop<DT, OP>(acc, n);
       for (int r = 0; r < n; ++r) reinterpret_cast<S*>(a.recv[r])[idx] = acc;
@@ -116,7 +115,8 @@ __global__ void __launch_bounds__(kOneShotThreads) oneShotKernel(const __grid_co
   {(const void*)oneShotKernel<DT, 0>, (const void*)oneShotKernel<DT, 1>, (const void*)oneShotKernel<DT, 2>, \
    (const void*)oneShotKernel<DT, 3>, (const void*)oneShotKernel<DT, 4>}
 
-extern const void* const kOneShot[4][5] = {VRCCL_ONESHOT_ROW(0), VRCCL_ONESHOT_ROW(1), VRCCL_ONESHOT_ROW(2),
-                                          VRCCL_ONESHOT_ROW(3)};
+extern const void* const kOneShot[vrcclNumTypes][5] = {
+    VRCCL_ONESHOT_ROW(0), VRCCL_ONESHOT_ROW(1), VRCCL_ONESHOT_ROW(2), VRCCL_ONESHOT_ROW(3),
+    VRCCL_ONESHOT_ROW(4), VRCCL_ONESHOT_ROW(5), VRCCL_ONESHOT_ROW(6), VRCCL_ONESHOT_ROW(7)};
 
 }  // namespace vrccl

@@ -25,21 +25,27 @@
 using namespace vrccl;
 
 namespace vrccl {
+// Types 0-3 and 4-7 of the two largest tables live in separate translation
+// units (compile time).
 extern const void* const kRingSimple[4][5];
 extern const void* const kTreeSimple[4][5];
-extern const void* const kRingLL[4][5];
-extern const void* const kTreeLL[4][5];
-extern const void* const kRingLL128[4][5];
-extern const void* const kTreeLL128[4][5];
+extern const void* const kRingSimpleX[4][5];
+extern const void* const kTreeSimpleX[4][5];
+extern const void* const kRingLL[vrcclNumTypes][5];
+extern const void* const kTreeLL[vrcclNumTypes][5];
+extern const void* const kRingLL128[vrcclNumTypes][5];
+extern const void* const kTreeLL128[vrcclNumTypes][5];
 extern const void* const kRingLL128W[4][5];
 extern const void* const kTreeLL128W[4][5];
-extern const void* const kOneShot[4][5];
-extern const void* const kGroupSimple[4][5];
-extern const void* const kGroupLL[4][5];
-extern const void* const kGroupLL128[4][5];
+extern const void* const kRingLL128WX[4][5];
+extern const void* const kTreeLL128WX[4][5];
+extern const void* const kOneShot[vrcclNumTypes][5];
+extern const void* const kGroupSimple[vrcclNumTypes][5];
+extern const void* const kGroupLL[vrcclNumTypes][5];
+extern const void* const kGroupLL128[vrcclNumTypes][5];
 
 const void* groupKernelFor(int proto, int dtype, int op) {
-  if (dtype < 0 || dtype >= 4 || op < 0 || op >= 5) return nullptr;
+  if (dtype < 0 || dtype >= vrcclNumTypes || op < 0 || op >= 5) return nullptr;
   switch (proto) {
     case kSimple: return kGroupSimple[dtype][op];
     case kLL: return kGroupLL[dtype][op];
@@ -49,16 +55,18 @@ const void* groupKernelFor(int proto, int dtype, int op) {
 }
 
 const void* kernelFor(int algo, int proto, int dtype, int op) {
-  if (dtype < 0 || dtype >= 4 || op < 0 || op >= 5) return nullptr;
+  if (dtype < 0 || dtype >= vrcclNumTypes || op < 0 || op >= 5) return nullptr;
+  const bool x = dtype >= 4;  // the second half of a split table
+  const int d = dtype & 3;
   switch (proto * 2 + algo) {
-    case kSimple * 2 + kRing: return kRingSimple[dtype][op];
-    case kSimple * 2 + kTree: return kTreeSimple[dtype][op];
+    case kSimple * 2 + kRing: return x ? kRingSimpleX[d][op] : kRingSimple[d][op];
+    case kSimple * 2 + kTree: return x ? kTreeSimpleX[d][op] : kTreeSimple[d][op];
     case kLL * 2 + kRing: return kRingLL[dtype][op];
     case kLL * 2 + kTree: return kTreeLL[dtype][op];
     case kLL128 * 2 + kRing: return kRingLL128[dtype][op];
     case kLL128 * 2 + kTree: return kTreeLL128[dtype][op];
-    case kLL128Wide * 2 + kRing: return kRingLL128W[dtype][op];
-    case kLL128Wide * 2 + kTree: return kTreeLL128W[dtype][op];
+    case kLL128Wide * 2 + kRing: return x ? kRingLL128WX[d][op] : kRingLL128W[d][op];
+    case kLL128Wide * 2 + kTree: return x ? kTreeLL128WX[d][op] : kTreeLL128W[d][op];
   }
   return nullptr;
 }
@@ -154,7 +162,7 @@ static bool envMasks(unsigned algoMask[3], unsigned protoMask[3]) {
 
 static const char* kAlgoName[4] = {"Ring", "Tree", "Auto", "OneShot"};
 static const char* kProtoName[3] = {"Simple", "LL", "LL128"};
-static const size_t kElemSize[4] = {4, 4, 2, 2};
+static const size_t kElemSize[vrcclNumTypes] = {4, 4, 2, 2, 1, 1, 8, 8};
 
 static size_t fifoBytes(int proto, int nranks, int maxCh) {
   return size_t(3) * maxCh * nranks * kSteps * slotBufferBytes(proto);

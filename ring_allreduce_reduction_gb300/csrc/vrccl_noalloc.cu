@@ -93,7 +93,7 @@ vrcclResult_t setupDevice(int dev, unsigned char** scratch) {
 extern "C" vrcclResult_t vrcclAllReduceNoAlloc(const void* const* sendbufs, void* const* recvbufs, size_t count,
                                                int nranks, vrcclDataType_t dtype, vrcclRedOp_t op,
                                                vrcclStream_t stream) {
-  static const size_t kElem[4] = {4, 4, 2, 2};
+  static const size_t kElem[vrcclNumTypes] = {4, 4, 2, 2, 1, 1, 8, 8};
   if (nranks < 1 || (unsigned)dtype >= (unsigned)vrcclNumTypes || (unsigned)op >= (unsigned)vrcclNumOps ||
       !sendbufs || !recvbufs)
     return vrcclInvalidArgument;

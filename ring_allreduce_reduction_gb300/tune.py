@@ -27,7 +27,7 @@ import time
 
 import torch
 
-ELEM = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+ELEM = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2, "int8": 1, "uint8": 1, "int64": 8, "float64": 8}
 TORCH = {"int32": torch.int32, "float32": torch.float32, "bfloat16": torch.bfloat16, "float16": torch.float16}
 
 

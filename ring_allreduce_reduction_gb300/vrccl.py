@@ -24,19 +24,20 @@ _lib = ctypes.CDLL(_LIB_PATH)
 
 RESULTS = ["vrcclSuccess", "vrcclInvalidArgument", "vrcclInvalidUsage", "vrcclInternalError",
            "vrcclCudaError", "vrcclTimeout", "vrcclAborted"]
-DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2, "float16": 3}
+DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2, "float16": 3, "int8": 4, "uint8": 5, "int64": 6, "float64": 7}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3, "avg": 4}
 ALGOS = {"ring": 0, "tree": 1, "auto": 2, "oneshot": 3}
 PROTOS = {"simple": 0, "ll": 1, "ll128": 2, "auto": 3}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 PROTO_NAMES = {v: k for k, v in PROTOS.items()}
-ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2}
+ELEM_SIZE = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2, "int8": 1, "uint8": 1, "int64": 8, "float64": 8}
 MAX_RANKS = 128
 MAX_CHANNELS = 64
 STEPS = 16
 
 _TORCH_DTYPES = {torch.int32: "int32", torch.float32: "float32", torch.bfloat16: "bfloat16",
-                 torch.float16: "float16"}
+                 torch.float16: "float16", torch.int8: "int8", torch.uint8: "uint8", torch.int64: "int64",
+                 torch.float64: "float64"}
 
 _c_int_p = ctypes.POINTER(ctypes.c_int)
 _sig = {

@@ -117,7 +117,11 @@ def test_binding_constants_match_the_header():
 
     dt = enum_body("vrcclInt32")
     assert {k: dt["vrccl" + {"int32": "Int32", "float32": "Float32", "bfloat16": "Bfloat16",
-                             "float16": "Float16"}[k]] for k in vrccl.DTYPES} == vrccl.DTYPES
+                             "float16": "Float16", "int8": "Int8", "uint8": "Uint8", "int64": "Int64",
+                             "float64": "Float64"}[k]] for k in vrccl.DTYPES} == vrccl.DTYPES
+    assert len(vrccl.DTYPES) == dt["vrcclNumTypes"]
+    from ring_allreduce_reduction_gb300 import workloads
+    assert set(workloads.DTYPES) == set(vrccl.DTYPES) and workloads.ELEM_SIZE == vrccl.ELEM_SIZE
     ops = enum_body("vrcclSum")
     assert {k: ops["vrccl" + k.capitalize()] for k in vrccl.OPS} == vrccl.OPS
     res = enum_body("vrcclSuccess")

@@ -227,7 +227,7 @@ def test_argument_errors(v):
         with pytest.raises(v.VrcclError, match="InvalidArgument"):  # rank 1's output overlaps rank 0's input
             v.vrcclAllReduce(s, [r[0], s[0] + 16], 64, "float32", "sum", "ring", "simple", comm)
         with pytest.raises(v.VrcclError, match="InvalidArgument"):
-            v.vrcclAllReduce(s, r, 64, 7, "sum", "ring", "simple", comm)
+            v.vrcclAllReduce(s, r, 64, len(v.DTYPES), "sum", "ring", "simple", comm)  # past the last type
         with pytest.raises(v.VrcclError, match="InvalidArgument"):
             v.vrcclCommSetSchedule(comm, 3, 0)  # more channels than the communicator has
     finally:
