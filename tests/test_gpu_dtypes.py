@@ -176,3 +176,23 @@ def test_new_dtypes_in_one_group(v):
             assert np.array_equal(y.view(np.uint8), ref.view(np.uint8)), (dt, op, s)
     finally:
         v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("algo", ["ring", "tree"])
+def test_new_dtypes_ll128_wide_kernels(v, algo):
+    """Four channels and 8 MiB per rank leave every agent many whole LL128
+    slices, so the wide LL128 kernels of types 4-7 run."""
+    n = 8
+    comm = v.vrcclCommInit(n, 4)
+    try:
+        v.vrcclCommSetSchedule(comm, 4, 0)
+        for dtype in NEW:
+            count = (8 << 20) // ELEM_SIZE[dtype] + 5
+            x = _inputs(n, count, dtype, "sum", seed=21)
+            y, s, b = run(v, comm, x, dtype, "sum", algo, "ll128")
+            assert s["proto"] == "ll128" and s["nchannels"] == 4
+            _parity(x, y, dtype, "sum", s)
+            assert b.canaries_intact()
+        assert v.vrcclCommGetAsyncError(comm) == 0
+    finally:
+        v.vrcclCommDestroy(comm)
