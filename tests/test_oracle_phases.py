@@ -21,16 +21,18 @@ import numpy as np
 import pytest
 
 from oracle import closed_form, phases, ring
-from ring_allreduce_reduction_gb300.workloads import make_inputs
+from ring_allreduce_reduction_gb300.workloads import ELEM_SIZE, make_inputs
 from tests.test_oracle_pins import _flatten_left_chain, _sym_combine
 
 OPS = ["sum", "prod", "max", "min", "avg"]
-DTYPES = ["int32", "float32", "bfloat16", "float16"]
+DTYPES = ["int32", "float32", "bfloat16", "float16", "int8", "uint8", "int64", "float64"]
+INT_RANGE = {"int32": (-2**20, 2**20), "int8": (-128, 127), "uint8": (0, 255), "int64": (-2**62, 2**62)}
 
 
 def _inputs(n, count, dtype, op, seed):
-    if dtype == "int32":
-        return make_inputs(n, count, dtype, "int_uniform", seed=seed, lo=-2**20, hi=2**20)
+    if dtype in INT_RANGE:
+        lo, hi = INT_RANGE[dtype]
+        return make_inputs(n, count, dtype, "int_uniform", seed=seed, lo=lo, hi=hi)
     if op == "prod":
         return make_inputs(n, count, dtype, "uniform", seed=seed, lo=0.5, hi=2.0)
     return make_inputs(n, count, dtype, "normal", seed=seed)
@@ -47,7 +49,7 @@ def test_reduce_scatter_matches_closed_form(dtype, op, n):
     for r in range(n):
         ok, worst = closed_form.check(y[r], x[:, r * b:(r + 1) * b], op, dtype)
         assert ok, (r, worst)
-        if dtype == "int32":
+        if dtype in INT_RANGE:
             assert np.array_equal(y[r], closed_form.exact(x[:, r * b:(r + 1) * b], op, dtype))
         # the predictor is a second route to the same bits
         p = phases.reduce_scatter_predict(x, op, dtype, r)
@@ -89,12 +91,13 @@ def test_all_gather_is_concatenation(n):
 
 
 @pytest.mark.parametrize("dtype,op", [("float32", "sum"), ("bfloat16", "sum"), ("float16", "avg"),
-                                      ("bfloat16", "max"), ("int32", "avg"), ("float32", "prod")])
+                                      ("bfloat16", "max"), ("int32", "avg"), ("float32", "prod"),
+                                      ("int8", "prod"), ("uint8", "avg"), ("int64", "sum"), ("float64", "avg")])
 @pytest.mark.parametrize("n", [2, 3, 5, 8])
 def test_allreduce_is_reduce_scatter_then_all_gather(dtype, op, n):
     """One channel, chunk = count/n (a multiple of 16 bytes): the AllReduce
     loop's chunks are the blocks, so the two step machines must agree."""
-    a = 16 // (4 if dtype in ("int32", "float32") else 2)
+    a = 16 // ELEM_SIZE[dtype]
     b = 24 * a
     x = _inputs(n, n * b, dtype, op, seed=11 + n)
     ar = ring.ring_allreduce(x, op, dtype, 1, b)
