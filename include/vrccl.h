@@ -29,14 +29,19 @@
  * algorithm reduces up and broadcasts down the double binary tree
  * [Architecture §5.4, §9.4; Deep Dive ch.4, ncclGetBtree/ncclGetDtree].
  *
- * Numerics. Floating ops are computed in binary32 (no contraction) and
- * rounded (to nearest even) to the element type after every step; int32
- * sum/prod wrap modulo 2^32. For the ring, an element of chunk j ends up as
+ * Numerics. Eight element types (vrcclDataType_t). bf16, fp16 and fp32 ops
+ * are computed in binary32 (no contraction) and rounded (to nearest even)
+ * to the element type after every step; fp64 ops are computed in binary64.
+ * Integer sum/prod (int8, uint8, int32, int64) wrap modulo 2^bits; max/min
+ * compare signed, unsigned for uint8. For the ring, an element of chunk j
+ * ends up as
  *   op(...op(op(x[j+1], x[j+2]), x[j+3])..., x[j])        (ranks mod n)
  * where the first operand is the value that arrived from the previous rank
  * and max/min keep the first operand on a tie. avg (not an NCCL op on the
- * pages): floats multiply every input once by 1.0f/n before the sum; int32
- * divides the wrapped sum by n, truncating toward zero, once per chunk.
+ * pages): the floating types multiply every input once by 1/n before the
+ * sum (the binary32 1.0f/n for bf16/fp16/fp32, the binary64 1.0/n for
+ * fp64); the integer types divide the wrapped sum by n, truncating toward
+ * zero, once per chunk.
  *
  * Ordering and concurrency. Every call is asynchronous on its stream and
  * returns once the work is enqueued [Deep Dive §1.3, "Step 2"]; results are
