@@ -16,8 +16,11 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "vrccl_internal.h"
 
@@ -41,51 +44,73 @@ static __device__ __align__(256) unsigned char gNoAllocScratch[kNoAllocScratchBy
 
 struct DeviceSetup {
   bool done;
-  vrcclResult_t result;
   unsigned char* scratch;  // device address of gNoAllocScratch on this device
+  unsigned long long timeoutNs;
 };
 DeviceSetup gSetup[kMaxDevices];
 std::mutex gSetupMu;
 
 // Once per device, with that device current: find the scratch's device
-// address, raise the shared-memory limit of the 20 ring/Simple kernels,
-// and check that the launch shape below is resident for the largest grid.
-vrcclResult_t setupDevice(int dev, unsigned char** scratch) {
+// address, raise the shared-memory limit of the 40 ring/Simple kernels,
+// check that the launch shape below is resident for the largest grid, and
+// read the wait limit (VRCCL_TIMEOUT_MS, as vrcclCommInit does). Only a
+// set-up that succeeded is kept: a failure that passes (a call made inside
+// a stream capture, say) is retried by the next call.
+vrcclResult_t setupDevice(int dev, unsigned char** scratch, unsigned long long* timeoutNs) {
   std::lock_guard<std::mutex> lk(gSetupMu);
   DeviceSetup& s = gSetup[dev];
   if (!s.done) {
-    s.done = true;
-    s.result = vrcclSuccess;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, gNoAllocScratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
-      s.result = vrcclCudaError;
-    } else {
-      s.scratch = static_cast<unsigned char*>(p);
-      int sms = 0, optin = 0;
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      // The same limit the communicator path sets for these kernels, so
-      // neither path lowers it for the other.
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-      for (int dt = 0; dt < vrcclNumTypes && s.result == vrcclSuccess; ++dt) {
-        for (int op = 0; op < vrcclNumOps && s.result == vrcclSuccess; ++op) {
-          const void* fn = kernelFor(kRing, kSimple, dt, op);
-          int per = 0;
-          if (!fn ||
-              cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024) !=
-                  cudaSuccess ||
-              cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, kNoAllocThreads, kNoAllocSmem) !=
-                  cudaSuccess ||
-              per * sms < kNoAllocMaxEdges) {
-            cudaGetLastError();
-            s.result = vrcclInternalError;
-          }
+      return vrcclCudaError;
+    }
+    int sms = 0, optin = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // The same limit the communicator path sets for these kernels, so
+    // neither path lowers it for the other.
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    for (int dt = 0; dt < vrcclNumTypes; ++dt) {
+      for (int op = 0; op < vrcclNumOps; ++op) {
+        const void* fn = kernelFor(kRing, kSimple, dt, op);
+        int per = 0;
+        if (!fn ||
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, kNoAllocThreads, kNoAllocSmem) !=
+                cudaSuccess ||
+            per * sms < kNoAllocMaxEdges) {
+          cudaGetLastError();
+          return vrcclInternalError;
         }
       }
     }
+    const char* tv = getenv("VRCCL_TIMEOUT_MS");
+    long long ms = tv && *tv ? atoll(tv) : 2000;
+    if (ms < 1) ms = 2000;
+    s.scratch = static_cast<unsigned char*>(p);
+    s.timeoutNs = (unsigned long long)ms * 1000000ull;
+    s.done = true;
   }
   *scratch = s.scratch;
-  return s.result;
+  *timeoutNs = s.timeoutNs;
+  return vrcclSuccess;
+}
+
+// The 2n buffers as byte ranges must not overlap, except that a rank's
+// recv buffer may be its own send buffer (in place), the rule of
+// vrcclAllReduce.
+bool overlapFree(const void* const* send, void* const* recv, int n, size_t bytes) {
+  std::vector<std::pair<uintptr_t, uintptr_t>> iv;
+  iv.reserve(2 * n);
+  for (int i = 0; i < n; ++i) {
+    const uintptr_t sb = (uintptr_t)send[i], rb = (uintptr_t)recv[i];
+    iv.push_back({sb, sb + bytes});
+    if (rb != sb) iv.push_back({rb, rb + bytes});
+  }
+  std::sort(iv.begin(), iv.end());
+  for (size_t i = 1; i < iv.size(); ++i)
+    if (iv[i].first < iv[i - 1].second) return false;
+  return true;
 }
 
 }  // namespace
@@ -105,10 +130,12 @@ extern "C" vrcclResult_t vrcclAllReduceNoAlloc(const void* const* sendbufs, void
   const size_t E = kElem[dtype];
   if (count > (size_t(1) << 40) / E) return vrcclInvalidArgument;
   if (count == 0) return vrcclSuccess;
+  if (!overlapFree(sendbufs, recvbufs, nranks, count * E)) return vrcclInvalidArgument;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return vrcclCudaError;
   unsigned char* scratch = nullptr;
-  vrcclResult_t r = setupDevice(dev, &scratch);
+  unsigned long long timeoutNs = 0;
+  vrcclResult_t r = setupDevice(dev, &scratch, &timeoutNs);
   if (r != vrcclSuccess) return r;
 
   // Every call starts from zeroed counters and status words (the FIFO slots
@@ -124,7 +151,7 @@ extern "C" vrcclResult_t vrcclAllReduceNoAlloc(const void* const* sendbufs, void
   ka.comm.status = reinterpret_cast<DevStatus*>(ctrl + kNoAllocCtrlBytes);
   ka.comm.devAbort = reinterpret_cast<int*>(ctrl + kNoAllocCtrlBytes + 128);
   ka.comm.hostAbort = reinterpret_cast<volatile int*>(ctrl + kNoAllocCtrlBytes + 192);
-  ka.comm.timeoutNs = 2000ull * 1000000ull;
+  ka.comm.timeoutNs = timeoutNs;
   ka.comm.nranks = nranks;
   ka.comm.maxChannels = std::max(1, std::min(4, kNoAllocMaxEdges / nranks));
   ka.comm.faultRank = ka.comm.faultChannel = -1;
