@@ -79,8 +79,21 @@ def max_over_ranks(x: float, device="cpu") -> float:
 
 
 def rank_seed(rank: int) -> int:
-    """Every GPU runs its own, differently seeded problem (weak scaling)."""
+    """The seed of GPU `rank`'s inputs: its shard of the one problem (or,
+    for the bucket and the phases, its own problem) is drawn from it."""
     return 1000 + rank
+
+
+def shard_of(v, count_per_gpu: int, dtype: str, world: int, rank: int):
+    """One problem split over the GPUs by element range (weak scaling: the
+    problem grows with the GPU count, each GPU's part stays the single-GPU
+    workload). Returns (global count per virtual rank, this GPU's first
+    element, its element count); the split is the library's
+    vrcclShardRange. The global input is the concatenation of the shards'
+    inputs, each drawn from its GPU's seed."""
+    total = count_per_gpu * world
+    off, ln = v.vrcclShardRange(total, dtype, world, rank)
+    return total, off, ln
 
 
 def busbw_gbs(bytes_per_rank: int, n: int, seconds: float, coll: str = "allreduce") -> float:
@@ -235,7 +248,13 @@ def run_reference(args) -> int:
     n, dtype = W["nranks"], W["dtype"]
     from oracle import ring as oring
     from ring_allreduce_reduction_gb300.workloads import make_inputs
-    nch, chunk = 1, 65536
+    # the schedule the GPU arm runs: the shipped tuning table's row for this
+    # workload (ring, Simple), chunk = VRCCL_STEPS/2 slices of the row's slice
+    from ring_allreduce_reduction_gb300.tune import read_table, table_choice
+    tpath = os.path.join(ROOT, "ring_allreduce_reduction_gb300", "tuning", f"gb300_n{n}.txt")
+    row = table_choice(read_table(tpath), n, W["bytes_per_rank"], ELEM[dtype], ("ring",), ("simple",),
+                       W["max_channels"]) if os.path.exists(tpath) else None
+    nch, chunk = (row["channels"], row["slice_bytes"] * 8 // ELEM[dtype]) if row else (1, 65536)
     probe = 1 << 20
     xp = make_inputs(n, probe, dtype, "uniform", seed=0)
     t0 = time.perf_counter()
@@ -370,6 +389,115 @@ def run_bucket(args) -> int:
     return 0
 
 
+def verify_download(x: np.ndarray, out: np.ndarray, op: str, dtype: str, nch: int, chunk: int, seed: int = 0,
+                    samples: int = 200_000) -> bool:
+    """Part of the CPU-baseline leg: a downloaded e2e result against the
+    oracle's ring association for the schedule that ran, on sampled
+    elements of every rank's buffer (and every rank equal to rank 0 there)."""
+    from oracle import ring as oring
+    n, count = x.shape
+    idx = np.unique(np.concatenate([np.random.default_rng(seed).choice(count, min(samples, count), replace=False),
+                                    [0, count - 1]]))
+    ref = oring.ring_predict(x, op, dtype, nch, chunk, idx)
+    return all(np.array_equal(out[r][idx].view(np.uint8), ref.view(np.uint8)) for r in range(n))
+
+
+def run_e2e(v, comm, x, recv, send, step, n, count, dtype, W, coll, world, stream, steps):
+    """The same metric end to end with pinned host buffers, in two forms,
+    both timed; the faster is reported, the other kept beside it.
+
+    serial     every step uploads the inputs, runs the collective and
+               downloads the result on one stream;
+    pipelined  (AllReduce) the buffers in 8 pieces, piece k+1's upload,
+               piece k's AllReduce and piece k-1's download overlapping on
+               three streams (the two copy directions run on separate copy
+               engines).
+    Returns the e2e record and, per form, the downloaded result with the
+    schedule it ran, which the CPU-baseline leg checks against the oracle."""
+    import torch
+    S = count * ELEM[dtype]
+    forms = {}
+    host_in = torch.from_numpy(x).pin_memory()
+    host_out = torch.empty(recv.shape, dtype=recv.dtype).pin_memory()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        send.copy_(host_in, non_blocking=True)
+        step()
+        host_out.copy_(recv, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, "cuda")
+    sched = v.vrcclCommGetLastSchedule(comm)
+    downloads = {}
+    if coll == "allreduce":
+        downloads["serial"] = [(x, host_out.numpy(), sched["nchannels"], sched["chunk_elems"])]
+    forms["serial"] = {"value": round(busbw_gbs(S, n, ms / 1e3, coll) * world, 3), "ms_per_step": round(ms, 3),
+                       "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
+                       "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "verified": None,
+                       "form": "serial: upload, AllReduce, download on one stream"}
+    del host_in
+    if coll == "allreduce" and count % 8 == 0:
+        K, pc = 8, count // 8
+        hin = torch.from_numpy(x).reshape(n, K, pc).permute(1, 0, 2).contiguous().pin_memory()  # [K, n, pc]
+        hout = torch.empty(hin.shape, dtype=hin.dtype).pin_memory()
+        dsend = torch.empty(hin.shape, dtype=hin.dtype, device="cuda")
+        drecv = torch.empty_like(dsend)
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(K)]
+        ev_red = [torch.cuda.Event() for _ in range(K)]
+        ev_out = [torch.cuda.Event() for _ in range(K)]
+        for k in range(K):  # events start completed
+            ev_red[k].record(stream)
+            ev_out[k].record(stream)
+
+        def pipe_step():
+            for k in range(K):
+                s_in.wait_event(ev_red[k])  # the previous step's AllReduce of piece k read dsend[k]
+                with torch.cuda.stream(s_in):
+                    dsend[k].copy_(hin[k], non_blocking=True)
+                ev_in[k].record(s_in)
+                stream.wait_event(ev_in[k])
+                stream.wait_event(ev_out[k])  # the previous step's download of drecv[k]
+                v.vrcclAllReduce([dsend[k, r] for r in range(n)], [drecv[k, r] for r in range(n)], pc, dtype,
+                                 W["op"], W["algo"], W["proto"], comm, stream)
+                ev_red[k].record(stream)
+                s_out.wait_event(ev_red[k])
+                with torch.cuda.stream(s_out):
+                    hout[k].copy_(drecv[k], non_blocking=True)
+                ev_out[k].record(s_out)
+
+        pipe_step()
+        torch.cuda.synchronize()
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(steps):
+            pipe_step()
+        stream.wait_event(ev_out[K - 1])
+        p1.record(stream)
+        torch.cuda.synchronize()
+        pms = max_over_ranks(p0.elapsed_time(p1) / steps, "cuda")
+        ps = v.vrcclCommGetLastSchedule(comm)
+        xk = x.reshape(n, K, pc)
+        hk = hout.numpy()  # [K, n, pc]
+        downloads["pipelined"] = [(np.ascontiguousarray(xk[:, k]), hk[k], ps["nchannels"], ps["chunk_elems"])
+                                  for k in range(K)]
+        forms["pipelined"] = {"value": round(busbw_gbs(S, n, pms / 1e3, coll) * world, 3),
+                              "ms_per_step": round(pms, 3), "h2d_bytes_per_step": hin.numel() * hin.element_size(),
+                              "d2h_bytes_per_step": hout.numel() * hout.element_size(), "verified": None,
+                              "form": f"pipelined: {K} pieces of {pc} elements per rank, upload / AllReduce / "
+                                      f"download on three streams"}
+        del hin, dsend, drecv
+    best = min(forms, key=lambda f: forms[f]["ms_per_step"])
+    e2e = {"value": forms[best]["value"], "unit": "GB/s", "h2d_bytes_per_step": forms[best]["h2d_bytes_per_step"],
+           "d2h_bytes_per_step": forms[best]["d2h_bytes_per_step"], "ms_per_step": forms[best]["ms_per_step"],
+           "form": best, "verified": None, "forms": forms}
+    return e2e, downloads
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -427,6 +555,12 @@ def main() -> int:
     S = W["bytes_per_rank"]
     count = S // ELEM[dtype]           # elements of the per-rank buffer that holds all n blocks
     block = count // n                 # phases: elements per block
+    shard = None
+    if coll == "allreduce" and world > 1:
+        # one AllReduce problem of world x S per virtual rank, split by
+        # element range: this GPU reduces its part of every rank's buffer
+        total, off, count = shard_of(v, count, dtype, world, rank)
+        shard = {"global_count_per_rank": total, "offset": off, "count": count}
     x = make_inputs(n, block if coll == "all_gather" else count, dtype, "uniform", seed=rank_seed(rank))
     send = torch.from_numpy(x).cuda()
     recv = torch.empty((n, block) if coll == "reduce_scatter" else (n, count), dtype=send.dtype, device=send.device)
@@ -500,79 +634,10 @@ def main() -> int:
                          "dram_frac_of_8tbs": round(dram / 8000.0, 4)})
 
     # ---- end to end through the public API with pinned host buffers
-    e2e = None
+    e2e, downloads = None, {}
     if not args.no_e2e:
-        host_in = torch.from_numpy(x).pin_memory()
-        host_out = torch.empty(recv.shape, dtype=recv.dtype).pin_memory()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            send.copy_(host_in, non_blocking=True)
-            step()
-            host_out.copy_(recv, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        e2e_ms = max_over_ranks(e2e_ms, "cuda")
-        e2e = {"value": round(busbw_gbs(S, n, e2e_ms / 1e3, coll) * world, 3), "unit": "GB/s",
-               "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
-               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": round(e2e_ms, 3),
-               "form": "serial: upload, AllReduce, download on one stream"}
-        del host_in, host_out
-        if coll == "allreduce" and count % 8 == 0:
-            # The same step as a user would pipeline it: the buffers in 8
-            # pieces, piece k+1's upload, piece k's AllReduce and piece
-            # k-1's download overlapping on three streams (the two copy
-            # directions run on separate copy engines).
-            K, pc = 8, count // 8
-            hin = torch.from_numpy(x).reshape(n, K, pc).permute(1, 0, 2).contiguous().pin_memory()  # [K, n, pc]
-            hout = torch.empty(hin.shape, dtype=hin.dtype).pin_memory()
-            dsend = torch.empty(hin.shape, dtype=hin.dtype, device="cuda")
-            drecv = torch.empty_like(dsend)
-            s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-            ev_in = [torch.cuda.Event() for _ in range(K)]
-            ev_red = [torch.cuda.Event() for _ in range(K)]
-            ev_out = [torch.cuda.Event() for _ in range(K)]
-            for k in range(K):  # events start completed
-                ev_red[k].record(stream)
-                ev_out[k].record(stream)
-
-            def pipe_step():
-                for k in range(K):
-                    s_in.wait_event(ev_red[k])  # the previous step's AllReduce of piece k read dsend[k]
-                    with torch.cuda.stream(s_in):
-                        dsend[k].copy_(hin[k], non_blocking=True)
-                    ev_in[k].record(s_in)
-                    stream.wait_event(ev_in[k])
-                    stream.wait_event(ev_out[k])  # the previous step's download of drecv[k]
-                    v.vrcclAllReduce([dsend[k, r] for r in range(n)], [drecv[k, r] for r in range(n)], pc, dtype,
-                                     W["op"], W["algo"], W["proto"], comm, stream)
-                    ev_red[k].record(stream)
-                    s_out.wait_event(ev_red[k])
-                    with torch.cuda.stream(s_out):
-                        hout[k].copy_(drecv[k], non_blocking=True)
-                    ev_out[k].record(s_out)
-
-            pipe_step()
-            torch.cuda.synchronize()
-            p0 = torch.cuda.Event(enable_timing=True)
-            p1 = torch.cuda.Event(enable_timing=True)
-            p0.record(stream)
-            for _ in range(args.e2e_steps):
-                pipe_step()
-            stream.wait_event(ev_out[K - 1])
-            p1.record(stream)
-            torch.cuda.synchronize()
-            pipe_ms = max_over_ranks(p0.elapsed_time(p1) / args.e2e_steps, "cuda")
-            ok = np.array_equal(hout[K - 1, 0].numpy().view(np.uint32)[:4], hout[K - 1, 1].numpy().view(np.uint32)[:4])
-            serial = e2e
-            e2e = {"value": round(busbw_gbs(S, n, pipe_ms / 1e3, coll) * world, 3), "unit": "GB/s",
-                   "h2d_bytes_per_step": hin.numel() * hin.element_size(),
-                   "d2h_bytes_per_step": hout.numel() * hout.element_size(), "ms_per_step": round(pipe_ms, 3),
-                   "form": f"pipelined: {K} pieces of {pc} elements per rank, upload / AllReduce / download on "
-                           f"three streams", "ranks_agree": bool(ok), "serial": serial}
+        e2e, downloads = run_e2e(v, comm, x, recv, send, step, n, count, dtype, W, coll, world, stream,
+                                 args.e2e_steps)
 
     # ---- the one-shot bound on the same buffers and schedule: every input
     # read once, every output written once, the ring's association order
@@ -603,6 +668,15 @@ def main() -> int:
     cpu = None
     if not args.no_cpu:
         cpu = cpu_baseline(x, dtype, W["op"], sched["nchannels"], sched["chunk_elems"], coll=coll)
+        # the e2e downloads against the oracle (sampled, per piece)
+        for form, pieces in downloads.items():
+            per = max(1, 200_000 // len(pieces))
+            e2e["forms"][form]["verified"] = all(
+                verify_download(xi, yi, W["op"], dtype, nch, ck, seed=k, samples=per)
+                for k, (xi, yi, nch, ck) in enumerate(pieces))
+        if e2e is not None:
+            e2e["verified"] = e2e["forms"][e2e["form"]]["verified"]
+        downloads.clear()
     line = {
         "metric": COLL_METRIC[coll], "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -613,7 +687,11 @@ def main() -> int:
                    "chunk_elems": sched["chunk_elems"], "blocks": shape["blocks"], "threads": shape["threads"],
                    "slice_elems": shape["slice_elems"],
                    "l2": "inputs larger than L2 (n*S = 2 GiB in, 2 GiB out); no flush",
-                   "algbw_gbs": round(S / (ms_step / 1e3) / 1e9 * world, 3)},
+                   "algbw_gbs": round(S / (ms_step / 1e3) / 1e9 * world, 3),
+                   "parallelism": (f"one problem split over {world} GPUs by element range (vrcclShardRange); "
+                                   f"no data-path collective" if shard else
+                                   f"{world} independent problems" if world > 1 else "single GPU"),
+                   "shard_rank0": shard},
         "kernel_ms": {"p10": round(float(np.percentile(kern_ms, 10)), 4),
                       "p50": round(float(np.percentile(kern_ms, 50)), 4),
                       "p90": round(float(np.percentile(kern_ms, 90)), 4)},

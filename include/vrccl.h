@@ -460,6 +460,24 @@ vrcclResult_t vrcclCommGetLaunchShape(vrcclComm_t comm, int* blocks, int* thread
 vrcclResult_t vrcclCommLoadTuning(vrcclComm_t comm, const char* path, int* loaded);
 
 /*
+ * vrcclShardRange -- the part of one virtual-rank problem that GPU `shard`
+ * of `nshards` computes, when the problem's element range is split across
+ * GPUs [Architecture §6.3: channels own independent contiguous ranges and
+ * never synchronise, so the channel partition of Deep Dive §2.2 applies one
+ * level up]. Parts are contiguous, in shard order, of alignUp(ceil(count /
+ * nshards), 16 bytes) elements; trailing parts may be short or empty. Each
+ * GPU holds the n virtual ranks' slices [offset, offset + length) of their
+ * buffers and runs vrcclAllReduce on them with a communicator of its own
+ * (no data moves between GPUs: the outputs are disjoint). Host only.
+ *   count    elements per virtual rank of the whole problem.
+ *   offset, length  out: the shard's first element and element count.
+ * Errors: vrcclInvalidArgument (bad dtype, nshards < 1, shard outside
+ * [0, nshards), null outputs).
+ */
+vrcclResult_t vrcclShardRange(size_t count, vrcclDataType_t dtype, int nshards, int shard, size_t* offset,
+                              size_t* length);
+
+/*
  * vrcclAllReduceNoAlloc -- the ring / Simple AllReduce of vrcclAllReduce,
  * for callers that cannot allocate device memory when they need it (code
  * running under a memory-pool manager that owns all of the device's
@@ -476,16 +494,20 @@ vrcclResult_t vrcclCommLoadTuning(vrcclComm_t comm, const char* path, int* loade
  * Memory: allocates nothing. Its scratch (FIFO slots, counters, status;
  * about 16 MiB) is one static device array that every GPU loading the
  * library holds until the process exits. The first call on a device looks
- * up that array's address and prepares the kernels; make that first call
- * before any stream capture. Every call then zeroes the counters and
- * status words on `stream` and launches one kernel; calls share the
- * array, so calls that overlap on the GPU (other streams, other host
- * threads) race and give undefined results -- order them.
+ * up that array's address, prepares the kernels and reads VRCCL_TIMEOUT_MS;
+ * make that first call before any stream capture (a set-up that fails is
+ * not kept: the next call tries again). Every call then zeroes the
+ * counters and status words on `stream` and launches one kernel; calls
+ * share the array, so calls that overlap on the GPU (other streams, other
+ * host threads) race and give undefined results -- order them.
  * Errors: vrcclInvalidArgument (null/misaligned pointers, bad enum,
- * nranks < 1); vrcclInvalidUsage (nranks > 32: the scratch is too small --
- * use a communicator); vrcclCudaError / vrcclInternalError (set-up or
- * launch failed). Device-side failures are not reported (there is no
- * communicator to ask); waits still give up after 2 s.
+ * nranks < 1, buffers that overlap other than in place); vrcclInvalidUsage
+ * (nranks > 32: the scratch is too small -- use a communicator);
+ * vrcclCudaError / vrcclInternalError (set-up or launch failed).
+ * Device-side failures are not reported (there is no communicator to
+ * ask): a wait still gives up after VRCCL_TIMEOUT_MS (default 2 s) and
+ * the kernel returns, but the call has already returned vrcclSuccess and
+ * the recv buffers are then undefined.
  */
 vrcclResult_t vrcclAllReduceNoAlloc(const void* const* sendbufs, void* const* recvbufs, size_t count, int nranks,
                                     vrcclDataType_t dtype, vrcclRedOp_t op, vrcclStream_t stream);

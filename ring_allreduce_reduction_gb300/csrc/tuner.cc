@@ -29,7 +29,8 @@ static int log2Bucket(size_t bytes) {
   return b;
 }
 
-Choice Tuner::choose(int nranks, size_t bytes, int maxChannels, unsigned algoMask, unsigned protoMask) const {
+Choice Tuner::choose(int nranks, size_t bytes, int esize, int maxChannels, unsigned algoMask,
+                     unsigned protoMask) const {
   // the size rule's preference order, first allowed protocol wins
   static const int kSmall[3] = {kLL, kLL128, kSimple}, kMid[3] = {kLL128, kSimple, kLL},
                    kLarge[3] = {kSimple, kLL128, kLL};
@@ -37,26 +38,47 @@ Choice Tuner::choose(int nranks, size_t bytes, int maxChannels, unsigned algoMas
   int proto = pref[0];
   for (int i = 2; i >= 0; --i)
     if (protoMask & (1u << pref[i])) proto = pref[i];
-  Choice c{(algoMask & (1u << kRing)) ? kRing : kTree, proto, 0, 0, 0};
+  Choice c{(algoMask & (1u << kRing)) ? kRing : kTree, proto, 0, 0, 0, false, 0, 0};
   auto eligible = [&](const Entry& e) {
     return e.nranks == nranks && e.channels <= maxChannels && (algoMask & (1u << e.algo)) &&
            (protoMask & (1u << e.proto));
   };
+  // The rows to use: those of the call's element size; else the rows that
+  // apply to any size; else those of the nearest measured element size
+  // (ties: the larger).
+  auto dist = [&](int s) { return std::abs(std::log2(double(s)) - std::log2(double(esize))); };
+  int group = -1;
+  for (const Entry& e : table_) {
+    if (!eligible(e)) continue;
+    if (e.esize == esize) {
+      group = esize;
+      break;
+    }
+    if (e.esize == 0) {
+      group = 0;
+    } else if (group != 0 && (group < 0 || dist(e.esize) < dist(group) ||
+                              (dist(e.esize) == dist(group) && e.esize > group))) {
+      group = e.esize;
+    }
+  }
+  if (group < 0) return c;
   const int want = log2Bucket(bytes);
   int bestDist = 1 << 30;
   for (const Entry& e : table_)
-    if (eligible(e)) bestDist = std::min(bestDist, std::abs(e.log2bytes - want));
-  if (bestDist == (1 << 30)) return c;
+    if (eligible(e) && e.esize == group) bestDist = std::min(bestDist, std::abs(e.log2bytes - want));
   double best = 1e300;
   for (const Entry& e : table_) {
     // the nearest measured size; the fastest entry there (ties keep the first)
-    if (!eligible(e) || std::abs(e.log2bytes - want) != bestDist) continue;
+    if (!eligible(e) || e.esize != group || std::abs(e.log2bytes - want) != bestDist) continue;
     if (e.us < best) {
       best = e.us;
       c.algo = e.algo;
       c.proto = e.proto;
       c.channels = e.channels;
       c.sliceBytes = e.sliceBytes;
+      c.measured = true;
+      c.esize = e.esize;
+      c.log2bytes = e.log2bytes;
     }
   }
   return c;
@@ -72,11 +94,14 @@ int Tuner::load(const char* path, int nranks) {
     if (hash) *hash = 0;
     Entry e;
     unsigned long long slice = 0;
-    if (sscanf(line, "%d %d %d %d %d %llu %lf", &e.nranks, &e.algo, &e.proto, &e.channels, &e.log2bytes, &slice,
-               &e.us) == 7) {
+    int esize = 0;
+    const int got = sscanf(line, "%d %d %d %d %d %llu %lf %d", &e.nranks, &e.algo, &e.proto, &e.channels,
+                           &e.log2bytes, &slice, &e.us, &esize);
+    if (got == 7 || got == 8) {
       e.sliceBytes = slice;
+      e.esize = got == 8 ? esize : 0;
       if (e.nranks == nranks && e.algo >= 0 && e.algo <= 1 && e.proto >= 0 && e.proto <= 2 && e.channels >= 1 &&
-          e.us > 0) {
+          e.us > 0 && (e.esize == 0 || e.esize == 1 || e.esize == 2 || e.esize == 4 || e.esize == 8)) {
         table_.push_back(e);
         ++count;
       }

@@ -512,6 +512,7 @@ struct Shape {
   size_t smem, sliceBytes, chunkBytes;
   const void* fn;
   int per;  // agents per channel
+  Choice tuned;  // what the tuning table (or the size rule) proposed
 };
 
 // Chooses algorithm, protocol and channels for `bytes` per rank (the tuning
@@ -535,7 +536,7 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
   if (userProto) protoMask = 1u << proto;
   if (algo == vrcclAlgoOneShot) protoMask = 1u << kSimple;
   if (!algoMask || !protoMask) return vrcclInvalidUsage;
-  Choice ch = comm->tuner.choose(n, bytes, comm->maxChannels, algoMask, protoMask);
+  Choice ch = comm->tuner.choose(n, bytes, (int)kE, comm->maxChannels, algoMask, protoMask);
   const int A = ch.algo, P = ch.proto;
   int C = comm->forceChannels ? comm->forceChannels
         : comm->envChannels   ? comm->envChannels
@@ -555,6 +556,7 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
     C = std::max(1, k * comm->smCount / per);
   }
   Shape s;
+  s.tuned = ch;
   s.A = A;
   s.P = P;
   s.fn = fn;
@@ -676,11 +678,16 @@ static void debugLine(vrcclComm_t comm, const char* what, size_t bytes, const ch
   if (!comm->debug) return;
   char host[64] = {0};
   gethostname(host, sizeof(host) - 1);
+  char src[64];
+  if (s.tuned.measured)
+    snprintf(src, sizeof(src), "measured (%d-byte rows, 2^%d B)", s.tuned.esize, s.tuned.log2bytes);
+  else
+    snprintf(src, sizeof(src), "size rule");
   fprintf(stderr,
           "%s:%d:%ld [%d] VRCCL INFO %s: %zu Bytes -> Algo %s proto %s channel{Lo..Hi}={0..%d} "
-          "chunk %zu slice %zu threads %d blocks %d nranks %d\n",
+          "chunk %zu slice %zu threads %d blocks %d nranks %d tuning %s\n",
           host, (int)getpid(), (long)syscall(SYS_gettid), comm->device, what, bytes, algoName, kProtoName[s.P],
-          s.C - 1, s.chunkBytes, s.sliceBytes, s.threads, blocks, comm->nranks);
+          s.C - 1, s.chunkBytes, s.sliceBytes, s.threads, blocks, comm->nranks, src);
 }
 
 // The one-shot AllReduce: C and the chunk as the ring/Simple schedule has
@@ -1091,3 +1098,23 @@ extern "C" vrcclResult_t vrcclModelPredict(const vrcclModelGraph_t* graph, vrccl
   return vrcclSuccess;
 }
 
+
+// Element-range sharding of one virtual-rank problem over several GPUs.
+// Channels own independent contiguous ranges and never synchronise with
+// each other ("NCCL architecture ...", §6.3), so the rule that cuts a
+// buffer into channel parts (parts of alignUp(ceil(count/C), 16 bytes)
+// elements, "NCCL Source Code Deep Dive", §2.2) cuts it into GPU parts one
+// level up; each GPU then runs the whole AllReduce on its part with the
+// schedule it chooses for that part.
+extern "C" vrcclResult_t vrcclShardRange(size_t count, vrcclDataType_t dtype, int nshards, int shard, size_t* offset,
+                                         size_t* length) {
+  if ((unsigned)dtype >= (unsigned)vrcclNumTypes || nshards < 1 || shard < 0 || shard >= nshards || !offset ||
+      !length)
+    return vrcclInvalidArgument;
+  const size_t A = 16 / kElemSize[dtype];
+  const size_t part = count ? ((count + nshards - 1) / nshards + A - 1) / A * A : 0;
+  const size_t lo = std::min(count, part * (size_t)shard);
+  *offset = lo;
+  *length = std::min(count, lo + part) - lo;
+  return vrcclSuccess;
+}

@@ -13,7 +13,10 @@ Usage (on the GPU):
         --min-bytes 8 --max-bytes 4194304 --out table.txt
 
 Table format (one entry per line, '#' comments):
-    nranks algo proto channels log2bytes sliceBytes microseconds
+    nranks algo proto channels log2bytes sliceBytes microseconds elementBytes
+(the library also reads lines without the last field, as rows for every
+element size). ``--append`` adds a sweep's rows to an existing table, so
+one table holds the sweeps of several element types.
 
     python -m ring_allreduce_reduction_gb300.tune --compare table.txt
 prints a table beside the pages' analytic model (no GPU needed).
@@ -121,18 +124,21 @@ def sweep(nranks: int, dtype: str, sizes: list[int], protos: list[str], algos: l
     return out
 
 
-def write_table(records: list[dict], path: str, header: str = "") -> None:
+def write_table(records: list[dict], path: str, header: str = "", append: bool = False) -> None:
     alg = {"ring": 0, "tree": 1}
     pro = {"simple": 0, "ll": 1, "ll128": 2}
-    with open(path, "w") as f:
-        f.write("# vrccl tuning table: nranks algo proto channels log2bytes sliceBytes microseconds\n")
+    fresh = not (append and os.path.exists(path))
+    with open(path, "w" if fresh else "a") as f:
+        if fresh:
+            f.write("# vrccl tuning table: nranks algo proto channels log2bytes sliceBytes microseconds "
+                    "elementBytes\n")
         if header:
             for ln in header.splitlines():
                 f.write(f"# {ln}\n")
         for r in records:
             log2 = max(0, int(r["bytes"]).bit_length() - 1)
             f.write(f"{r['nranks']} {alg[r['algo']]} {pro[r['proto']]} {r['channels']} {log2} {r['slice_bytes']} "
-                    f"{r['us']:.3f}\n")
+                    f"{r['us']:.3f} {ELEM[r['dtype']] if 'dtype' in r else 0}\n")
 
 
 def read_table(path: str) -> list[dict]:
@@ -141,11 +147,41 @@ def read_table(path: str) -> list[dict]:
     recs = []
     for ln in open(path):
         ln = ln.split("#", 1)[0].split()
-        if len(ln) == 7:
-            n, a, p, c, lg, sl, us = ln
+        if len(ln) in (7, 8):
+            n, a, p, c, lg, sl, us = ln[:7]
             recs.append({"nranks": int(n), "algo": alg[int(a)], "proto": pro[int(p)], "channels": int(c),
-                         "bytes": 1 << int(lg), "slice_bytes": int(sl), "us": float(us)})
+                         "bytes": 1 << int(lg), "slice_bytes": int(sl), "us": float(us),
+                         "esize": int(ln[7]) if len(ln) == 8 else 0})
     return recs
+
+
+def table_choice(recs: list[dict], nranks: int, nbytes: int, esize: int, algos=("ring", "tree"),
+                 protos=("simple", "ll", "ll128"), max_channels: int = 64) -> dict | None:
+    """The row the library's tuner takes for a call (host only, for tools
+    that need the schedule without a GPU): the rows of the call's element
+    size (else rows for any size, else the nearest measured element size),
+    the nearest measured power-of-two size, the fastest row there. None
+    if the table has no eligible row."""
+    import math
+    el = [r for r in recs if r["nranks"] == nranks and r["channels"] <= max_channels and r["algo"] in algos
+          and r["proto"] in protos]
+    if not el:
+        return None
+    sizes = {r.get("esize", 0) for r in el}
+    if esize in sizes:
+        g = esize
+    elif 0 in sizes:
+        g = 0
+    else:
+        g = min(sizes, key=lambda e: (abs(math.log2(e) - math.log2(esize)), -e))
+    el = [r for r in el if r.get("esize", 0) == g]
+    b = max(0, int(nbytes).bit_length() - 1)
+    if b < 62 and nbytes - (1 << b) > (1 << (b + 1)) - nbytes:
+        b += 1
+    want = 1 << b
+    d = min(abs(r["bytes"].bit_length() - want.bit_length()) for r in el)
+    here = [r for r in el if abs(r["bytes"].bit_length() - want.bit_length()) == d]
+    return min(here, key=lambda r: r["us"])
 
 
 def compare(recs: list[dict], arch: str = "blackwell", hw: str = "nvlink") -> list[dict]:
@@ -203,6 +239,7 @@ def main() -> int:
     ap.add_argument("--max-channels", type=int, default=32)
     ap.add_argument("--iters", type=int, default=30)
     ap.add_argument("--out", default="")
+    ap.add_argument("--append", action="store_true", help="add the rows to the --out table instead of replacing it")
     ap.add_argument("--json", default="")
     ap.add_argument("--graph", action="store_true",
                     help="time 1000 calls captured in a CUDA graph per point (device latency, no launch overhead)")
@@ -221,7 +258,7 @@ def main() -> int:
                  graph=args.graph)
     if args.out:
         write_table(recs, args.out, header=f"measured on {torch.cuda.get_device_name()} in {time.time() - t0:.0f} s, "
-                                           f"dtype {args.dtype}, op {args.op}")
+                                           f"dtype {args.dtype}, op {args.op}", append=args.append)
     if args.json:
         import json
         with open(args.json, "w") as f:

@@ -68,6 +68,8 @@ _sig = {
     "vrcclCommInjectFault": [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int],
     "vrcclCommGetLaunchShape": [ctypes.c_void_p, _c_int_p, _c_int_p, _c_int_p],
     "vrcclCommLoadTuning": [ctypes.c_void_p, ctypes.c_char_p, _c_int_p],
+    "vrcclShardRange": [ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t),
+                        ctypes.POINTER(ctypes.c_size_t)],
     "vrcclAllReduceNoAlloc": [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t,
                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p],
 }
@@ -157,6 +159,15 @@ def vrcclAllReduceNoAlloc(sendbufs, recvbufs, count: int, nranks: int, dtype, op
     R = (ctypes.c_void_p * len(recvbufs))(*[_ptr(b) for b in recvbufs])
     _check(_lib.vrcclAllReduceNoAlloc(S, R, count, nranks, _enum(DTYPES, dtype, "dtype"), _enum(OPS, op, "op"),
                                       _stream(stream)), "vrcclAllReduceNoAlloc")
+
+
+def vrcclShardRange(count: int, dtype, nshards: int, shard: int) -> tuple[int, int]:
+    """(offset, length) of GPU `shard`'s part of a problem split over
+    `nshards` GPUs by element range (host only; see include/vrccl.h)."""
+    off, ln = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_lib.vrcclShardRange(count, _enum(DTYPES, dtype, "dtype"), nshards, shard, ctypes.byref(off),
+                                ctypes.byref(ln)), "vrcclShardRange")
+    return off.value, ln.value
 
 
 def vrcclGroupStart() -> None:

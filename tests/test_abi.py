@@ -73,24 +73,34 @@ def test_binding_names_match_the_c_names():
 
 def test_tuning_table_writer_format(tmp_path):
     """tune.write_table emits the line format the library parses:
-    nranks algo proto channels log2bytes sliceBytes microseconds."""
-    from ring_allreduce_reduction_gb300.tune import write_table
-    recs = [{"nranks": 8, "algo": "tree", "proto": "ll128", "channels": 3, "bytes": 1 << 20, "slice_bytes": 30720,
-             "us": 12.5}]
+    nranks algo proto channels log2bytes sliceBytes microseconds
+    elementBytes; --append adds rows under the first header."""
+    pytest.importorskip("torch")
+    from ring_allreduce_reduction_gb300.tune import read_table, write_table
+    recs = [{"nranks": 8, "dtype": "bfloat16", "algo": "tree", "proto": "ll128", "channels": 3, "bytes": 1 << 20,
+             "slice_bytes": 30720, "us": 12.5}]
     p = tmp_path / "t.txt"
     write_table(recs, str(p), header="x")
+    write_table([dict(recs[0], dtype="float32", us=7.25)], str(p), header="y", append=True)
     rows = [ln.split() for ln in p.read_text().splitlines() if not ln.startswith("#")]
-    assert rows == [["8", "1", "2", "3", "20", "30720", "12.500"]]
+    assert rows == [["8", "1", "2", "3", "20", "30720", "12.500", "2"], ["8", "1", "2", "3", "20", "30720", "7.250", "4"]]
+    assert [r["esize"] for r in read_table(str(p))] == [2, 4]
 
 
-def test_shipped_tuning_table_parses():
-    path = os.path.join(ROOT, "ring_allreduce_reduction_gb300", "tuning", "gb300_n8.txt")
-    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
-    assert len(rows) > 100
-    for r in rows:
-        n, algo, proto, ch, lg, sl = map(int, r[:6])
-        assert n == 8 and algo in (0, 1) and proto in (0, 1, 2) and 1 <= ch <= 64 and 0 <= lg < 40 and sl > 0
-        assert float(r[6]) > 0
+def test_shipped_tuning_tables_parse():
+    d = os.path.join(ROOT, "ring_allreduce_reduction_gb300", "tuning")
+    tables = sorted(f for f in os.listdir(d) if re.fullmatch(r"gb300_n\d+\.txt", f))
+    assert "gb300_n8.txt" in tables
+    for f in tables:
+        nr = int(re.findall(r"\d+", f)[1])
+        rows = [ln.split() for ln in open(os.path.join(d, f)) if ln.strip() and not ln.startswith("#")]
+        assert len(rows) > 50, f
+        for r in rows:
+            assert len(r) in (7, 8), (f, r)
+            n, algo, proto, ch, lg, sl = map(int, r[:6])
+            assert n == nr and algo in (0, 1) and proto in (0, 1, 2) and 1 <= ch <= 64 and 0 <= lg < 40 and sl > 0
+            assert float(r[6]) > 0
+            assert len(r) == 7 or int(r[7]) in (1, 2, 4, 8)
 
 
 def test_binding_constants_match_the_header():
@@ -139,3 +149,26 @@ def test_group_depth_on_the_host(lib):
     assert lib.vrcclGroupEnd() == 2
     bogus = ctypes.create_string_buffer(4096)
     assert lib.vrcclCommGetGroupSchedule(bogus, 0, None, None, None, None, None) == 1
+
+
+def test_no_alloc_host_checks(lib):
+    """vrcclAllReduceNoAlloc refuses bad arguments before touching a GPU:
+    too many ranks, misaligned pointers, and buffers that overlap other
+    than in place (the pointers below are never dereferenced)."""
+    P = ctypes.c_void_p
+    base = 1 << 40
+
+    def call(send, recv, count, n, dtype=1, op=0):
+        s = (P * n)(*send)
+        r = (P * n)(*recv)
+        return lib.vrcclAllReduceNoAlloc(s, r, ctypes.c_size_t(count), n, dtype, op, None)
+
+    n, count = 4, 1024  # 4 KiB per rank
+    send = [base + i * 8192 for i in range(n)]
+    assert call([base] * 33, [base + 8192] * 33, count, 33) == 2                      # beyond the scratch
+    assert call([s + 8 for s in send], send, count, n) == 1                          # misaligned
+    assert call(send, [s + 4096 - 16 for s in send], count, n) == 1                  # recv overlaps a send buffer
+    assert call(send, [base + 65536] * n, count, n) == 1                             # recv buffers overlap each other
+    assert call(send, send, 0, n) == 0                                               # count 0: nothing to do
+    assert call([], [], count, 0) == 1                                               # no ranks
+    assert call(send, send, count, n, dtype=8) == 1                                  # bad type

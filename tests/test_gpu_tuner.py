@@ -119,3 +119,43 @@ def test_env_lists_steer_auto(v, monkeypatch):
     with pytest.raises(v.VrcclError) as e:
         v.vrcclCommInit(n, 8)
     assert e.value.name == "vrcclInvalidArgument"
+
+
+def test_element_size_picks_its_own_rows(v, tmp_path, monkeypatch, capfd):
+    """A table keyed by element size: a bf16 call and an fp32 call of the
+    same byte size take their own rows; a type the table has no rows for
+    takes the rows of the nearest measured element size. The decision line
+    (VRCCL_DEBUG=INFO) names the rows used."""
+    n = 5
+    table = tmp_path / "table.txt"
+    # nranks algo proto channels log2bytes sliceBytes us elementBytes; 2^18 B per rank
+    table.write_text("5 1 2 3 18 30720 5.0 2\n"    # bf16: tree ll128 C=3
+                     "5 0 0 2 18 16384 9.0 2\n"
+                     "5 0 0 2 18 16384 4.0 4\n"    # fp32: ring simple C=2
+                     "5 1 2 3 18 30720 6.0 4\n")
+    monkeypatch.setenv("VRCCL_DEBUG", "INFO")
+    comm = v.vrcclCommInit(n, 4)
+    try:
+        assert v.vrcclCommLoadTuning(comm, str(table)) == 4
+        for dtype, count, want in (("bfloat16", 1 << 17, ("tree", "ll128", 3)),
+                                   ("float32", 1 << 16, ("ring", "simple", 2)),
+                                   ("int8", 1 << 18, ("tree", "ll128", 3)),      # nearest rows: 2-byte
+                                   ("float64", 1 << 15, ("ring", "simple", 2))):  # nearest rows: 4-byte
+            if dtype == "int8":
+                x = make_inputs(n, count, dtype, "int_uniform", seed=5, lo=-128, hi=127)
+            else:
+                x = make_inputs(n, count, dtype, "normal", seed=5)
+            y, sched, _ = run(v, comm, x, dtype, "sum", "auto", "auto")
+            assert (sched["algo"], sched["proto"], sched["nchannels"]) == want, (dtype, sched)
+            if sched["algo"] == "tree":
+                ref = otree.tree_allreduce(x, "sum", dtype, sched["nchannels"])
+            else:
+                ref = oring.ring_allreduce(x, "sum", dtype, sched["nchannels"], sched["chunk_elems"])
+            assert np.array_equal(y.view(np.uint8), ref.view(np.uint8)), dtype
+        err = capfd.readouterr().err
+        lines = [ln for ln in err.splitlines() if "VRCCL INFO AllReduce" in ln]
+        assert len(lines) == 4
+        assert "measured (2-byte rows, 2^18 B)" in lines[0] and "measured (4-byte rows, 2^18 B)" in lines[1]
+        assert "measured (2-byte rows" in lines[2] and "measured (4-byte rows" in lines[3]
+    finally:
+        v.vrcclCommDestroy(comm)
