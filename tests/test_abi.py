@@ -172,3 +172,27 @@ def test_no_alloc_host_checks(lib):
     assert call(send, send, 0, n) == 0                                               # count 0: nothing to do
     assert call([], [], count, 0) == 1                                               # no ranks
     assert call(send, send, count, n, dtype=8) == 1                                  # bad type
+
+
+def test_table_choice_mirrors_the_rule():
+    """tune.table_choice, the host mirror of the library's rule: rows of the
+    call's element size, else rows for any size, else the nearest measured
+    element size (ties to the larger); then the nearest power-of-two size
+    and the fastest row there."""
+    pytest.importorskip("torch")
+    from ring_allreduce_reduction_gb300.tune import table_choice
+    def row(algo, proto, ch, lg, us, es):
+        return {"nranks": 5, "algo": algo, "proto": proto, "channels": ch, "bytes": 1 << lg, "slice_bytes": 16384,
+                "us": us, "esize": es}
+    t = [row("tree", "ll128", 3, 18, 5.0, 2), row("ring", "simple", 2, 18, 9.0, 2),
+         row("ring", "simple", 2, 18, 4.0, 4), row("tree", "ll128", 3, 18, 6.0, 4),
+         row("ring", "ll", 1, 10, 1.0, 4)]
+    pick = lambda **kw: (lambda r: (r["algo"], r["proto"], r["channels"]))(table_choice(t, **kw))
+    assert pick(nranks=5, nbytes=1 << 18, esize=2) == ("tree", "ll128", 3)
+    assert pick(nranks=5, nbytes=1 << 18, esize=4) == ("ring", "simple", 2)
+    assert pick(nranks=5, nbytes=1 << 18, esize=1) == ("tree", "ll128", 3)      # nearest: 2-byte rows
+    assert pick(nranks=5, nbytes=1 << 18, esize=8) == ("ring", "simple", 2)     # nearest: 4-byte rows
+    assert pick(nranks=5, nbytes=300 << 10, esize=4) == ("ring", "simple", 2)   # nearest size 2^18
+    assert pick(nranks=5, nbytes=1000, esize=4) == ("ring", "ll", 1)
+    assert pick(nranks=5, nbytes=1 << 18, esize=4, protos=("ll128",)) == ("tree", "ll128", 3)
+    assert table_choice(t, nranks=6, nbytes=1 << 18, esize=4) is None

@@ -54,17 +54,28 @@ def test_auto_follows_the_measured_table(v, tmp_path):
         v.vrcclCommDestroy(comm)
 
 
-def test_shipped_table_is_found_for_8_ranks(v):
-    from ring_allreduce_reduction_gb300 import vrccl
-    path = os.path.join(os.path.dirname(vrccl.LIB_PATH), "tuning", "gb300_n8.txt")
+@pytest.mark.parametrize("n", [4, 8, 16, 32, 72])
+def test_shipped_tables_drive_auto(v, n, monkeypatch, capfd):
+    """Every configured rank count has a shipped table: "auto" takes the
+    row the table rule names (the host mirror in tune.table_choice), the
+    decision line says the choice was measured, and the result is the
+    oracle's."""
+    from ring_allreduce_reduction_gb300 import tune, vrccl
+    path = os.path.join(os.path.dirname(vrccl.LIB_PATH), "tuning", f"gb300_n{n}.txt")
     assert os.path.exists(path)
-    comm = v.vrcclCommInit(8, 32)
+    rows = tune.read_table(path)
+    monkeypatch.setenv("VRCCL_DEBUG", "INFO")
+    comm = v.vrcclCommInit(n, 64)
     try:
-        # tiny message: the measured table says LL (ring or tree), not Simple
-        x = make_inputs(8, 64, "float32", "normal", seed=4)
-        y, sched, _ = run(v, comm, x, "float32", "sum", "auto", "auto")
-        assert sched["proto"] == "ll"
-        _check(x, y, sched)
+        for count in (64, 1 << 14, 1 << 17):
+            x = make_inputs(n, count, "float32", "normal", seed=4)
+            y, sched, _ = run(v, comm, x, "float32", "sum", "auto", "auto")
+            want = tune.table_choice(rows, n, count * 4, 4)
+            assert (sched["algo"], sched["proto"]) == (want["algo"], want["proto"]), (count, sched, want)
+            _check(x, y, sched)
+        err = capfd.readouterr().err
+        lines = [ln for ln in err.splitlines() if "VRCCL INFO AllReduce" in ln]
+        assert len(lines) == 3 and all("tuning measured (4-byte rows" in ln for ln in lines), lines
     finally:
         v.vrcclCommDestroy(comm)
 
