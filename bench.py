@@ -211,29 +211,99 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---- the CPU oracle on the host cores: channels are independent ranges
+# ("NCCL architecture ...", §6.3), so each worker process runs the oracle,
+# unchanged, on one channel's part of every rank's buffer with one channel
+# (the loops of a channel are cut relative to its own start, so the part's
+# result is the whole run's). Inputs and outputs sit in shared memory.
+_POOL_STATE = {}
+
+
+def _pool_attach(in_name, out_name, shape, np_dtype):
+    from multiprocessing import shared_memory
+    shm_in = shared_memory.SharedMemory(name=in_name)
+    shm_out = shared_memory.SharedMemory(name=out_name)
+    _POOL_STATE.update(shm_in=shm_in, shm_out=shm_out,
+                       x=np.ndarray(shape, dtype=np_dtype, buffer=shm_in.buf),
+                       y=np.ndarray(shape, dtype=np_dtype, buffer=shm_out.buf))
+
+
+def _pool_channel(task):
+    from oracle import ring as oring
+    lo, hi, op, dtype, chunk = task
+    x, y = _POOL_STATE["x"], _POOL_STATE["y"]
+    if hi > lo:
+        y[:, lo:hi] = oring.ring_allreduce(np.ascontiguousarray(x[:, lo:hi]), op, dtype, 1, chunk)
+    return hi - lo
+
+
+class ParallelOracle:
+    """The ring oracle over the channels of one schedule, one worker
+    process per host core (at most one per channel)."""
+
+    def __init__(self, x: np.ndarray, dtype: str, op: str, nch: int, chunk: int):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        from oracle import schedule
+        self.shape, self.np_dtype = x.shape, x.dtype
+        self.shm_in = shared_memory.SharedMemory(create=True, size=max(1, x.nbytes))
+        self.shm_out = shared_memory.SharedMemory(create=True, size=max(1, x.nbytes))
+        np.ndarray(x.shape, dtype=x.dtype, buffer=self.shm_in.buf)[...] = x
+        self.y = np.ndarray(x.shape, dtype=x.dtype, buffer=self.shm_out.buf)
+        ranges = schedule.channel_ranges(x.shape[1], nch, ELEM[dtype])
+        self.tasks = [(lo, hi, op, dtype, chunk) for lo, hi in ranges]
+        self.cores = max(1, min(len(self.tasks), os.cpu_count() or 1))
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_pool_attach,
+                                                 initargs=(self.shm_in.name, self.shm_out.name, x.shape, x.dtype))
+        self.pool.map(_pool_channel, [(0, 0, op, dtype, chunk)] * self.cores)  # workers up before timing
+
+    def run(self) -> np.ndarray:
+        self.pool.map(_pool_channel, self.tasks, chunksize=1)
+        return self.y
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        for shm in (self.shm_in, self.shm_out):
+            shm.close()
+            shm.unlink()
+
+
 def cpu_baseline(x: np.ndarray, dtype: str, op: str, nch: int, chunk_elems: int, min_seconds: float = 10.0,
                  coll: str = "allreduce") -> dict:
     """The oracle as it stands on the bench's own inputs, replaying the
-    schedule the GPU ran (same channels and chunk), repeated until about
-    `min_seconds` of CPU time (at most 40 runs)."""
-    from oracle import phases, ring as oring
+    schedule the GPU ran (same channels and chunk) on the host cores (one
+    process per channel, up to the core count), repeated until about
+    `min_seconds` of wall time (at most 40 runs). The phases run on one
+    core (their oracle has no channels)."""
+    from oracle import phases
     n, count = x.shape
-    run = {"allreduce": lambda: oring.ring_allreduce(x, op, dtype, nch, chunk_elems),
-           "reduce_scatter": lambda: phases.ring_reduce_scatter(x, op, dtype),
-           "all_gather": lambda: phases.ring_all_gather(x)}[coll]
+    par = None
+    if coll == "allreduce":
+        par = ParallelOracle(x, dtype, op, nch, chunk_elems)
+        run, cores = par.run, par.cores
+    else:
+        run = {"reduce_scatter": lambda: phases.ring_reduce_scatter(x, op, dtype),
+               "all_gather": lambda: phases.ring_all_gather(x)}[coll]
+        cores = 1
     times = []
-    while True:
-        t0 = time.perf_counter()
-        run()
-        times.append(time.perf_counter() - t0)
-        if sum(times) >= min_seconds or len(times) >= 40:
-            break
+    try:
+        while True:
+            t0 = time.perf_counter()
+            run()
+            times.append(time.perf_counter() - t0)
+            if sum(times) >= min_seconds or len(times) >= 40:
+                break
+    finally:
+        if par is not None:
+            par.close()
     dt = statistics.mean(times)
     S = count * ELEM[dtype] * (n if coll == "all_gather" else 1)
-    return {"value": round(busbw_gbs(S, n, dt, coll), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    how = (f"numpy step machine, one process per channel on {cores} host cores" if par is not None
+           else "numpy step machine, one thread")
+    return {"value": round(busbw_gbs(S, n, dt, coll), 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"the whole workload: n={n} x {count} {dtype} per rank send buffer, {coll}, {nch} channels, "
-                      f"chunk {chunk_elems} elements; numpy step machine, one thread; {len(times)} run(s), "
-                      f"mean {dt:.2f} s"}
+                      f"chunk {chunk_elems} elements; {how}; {len(times)} run(s), mean {dt:.2f} s"}
 
 
 def run_reference(args) -> int:
@@ -259,18 +329,23 @@ def run_reference(args) -> int:
     xp = make_inputs(n, probe, dtype, "uniform", seed=0)
     t0 = time.perf_counter()
     oring.ring_allreduce(xp, W["op"], dtype, nch, chunk)
-    per_elem = (time.perf_counter() - t0) / probe
+    cores = max(1, min(nch, os.cpu_count() or 1))
+    per_elem = (time.perf_counter() - t0) / probe / cores  # roughly: the channels run on `cores` processes
     per_step = args.ref_budget / max(1, args.steps + args.warmup)
     full = W["bytes_per_rank"] // ELEM[dtype]
     count = int(min(full, max(1 << 16, per_step / max(per_elem, 1e-12)))) // 4 * 4
     x = make_inputs(n, count, dtype, "uniform", seed=0)
-    for _ in range(args.warmup):
-        oring.ring_allreduce(x, W["op"], dtype, nch, chunk)
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oring.ring_allreduce(x, W["op"], dtype, nch, chunk)
-        times.append(time.perf_counter() - t0)
+    par = ParallelOracle(x, dtype, W["op"], nch, chunk)
+    try:
+        for _ in range(args.warmup):
+            par.run()
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            par.run()
+            times.append(time.perf_counter() - t0)
+    finally:
+        par.close()
     S = count * ELEM[dtype]
     mean = statistics.mean(times)
     v = busbw_gbs(S, n, mean)
@@ -281,9 +356,10 @@ def run_reference(args) -> int:
         "config": {"workload": W["name"], "nranks": n, "bytes_per_rank": W["bytes_per_rank"],
                    "sample_bytes_per_rank": S, "op": W["op"], "algo": "ring", "channels": nch,
                    "chunk_elems": chunk},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": par.cores, "kind": "oracle",
                          "sample": f"per step n={n} x {count} {dtype} per rank ({S >> 20} MiB/rank) of the "
-                                   f"{W['bytes_per_rank'] >> 20} MiB/rank workload; numpy step machine, one thread"},
+                                   f"{W['bytes_per_rank'] >> 20} MiB/rank workload; numpy step machine, one "
+                                   f"process per channel on {par.cores} host cores"},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -389,6 +465,12 @@ def run_bucket(args) -> int:
     return 0
 
 
+def _host(x: np.ndarray) -> np.ndarray:
+    """bf16 storage (uint16 bit patterns) as int16, which torch moves and
+    pins like any 2-byte type."""
+    return x.view(np.int16) if x.dtype == np.uint16 else x
+
+
 def verify_download(x: np.ndarray, out: np.ndarray, op: str, dtype: str, nch: int, chunk: int, seed: int = 0,
                     samples: int = 200_000) -> bool:
     """Part of the CPU-baseline leg: a downloaded e2e result against the
@@ -417,7 +499,7 @@ def run_e2e(v, comm, x, recv, send, step, n, count, dtype, W, coll, world, strea
     import torch
     S = count * ELEM[dtype]
     forms = {}
-    host_in = torch.from_numpy(x).pin_memory()
+    host_in = torch.from_numpy(_host(x)).pin_memory()
     host_out = torch.empty(recv.shape, dtype=recv.dtype).pin_memory()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -441,7 +523,7 @@ def run_e2e(v, comm, x, recv, send, step, n, count, dtype, W, coll, world, strea
     del host_in
     if coll == "allreduce" and count % 8 == 0:
         K, pc = 8, count // 8
-        hin = torch.from_numpy(x).reshape(n, K, pc).permute(1, 0, 2).contiguous().pin_memory()  # [K, n, pc]
+        hin = torch.from_numpy(_host(x)).reshape(n, K, pc).permute(1, 0, 2).contiguous().pin_memory()  # [K, n, pc]
         hout = torch.empty(hin.shape, dtype=hin.dtype).pin_memory()
         dsend = torch.empty(hin.shape, dtype=hin.dtype, device="cuda")
         drecv = torch.empty_like(dsend)
@@ -517,6 +599,10 @@ def main() -> int:
                     help="ring AllReduce with the direct all-gather (through the recv buffers)")
     ap.add_argument("--bucket", default="", choices=["", "flat", "group", "separate"],
                     help="time the 224-tensor bf16 gradient bucket instead of the workload")
+    ap.add_argument("--proto", default="", choices=["", "simple", "ll", "ll128"],
+                    help="profiling only: another protocol than the workload's (named in config)")
+    ap.add_argument("--dtype", default="", choices=["", "float32", "bfloat16"],
+                    help="profiling only: another element type than the workload's (named in config)")
     ap.add_argument("--bytes-per-rank", type=int, default=0,
                     help="profiling only: a smaller per-rank size than the workload's (reported in config)")
     args = ap.parse_args()
@@ -548,6 +634,12 @@ def main() -> int:
     elif args.algo != "ring":
         W["algo"] = args.algo
         W["name"] = W["name"].replace("_ring_", "_" + args.algo + "_")
+    if args.proto and args.proto != W["proto"]:
+        W["proto"] = args.proto
+        W["name"] = W["name"].replace("_simple_", "_" + args.proto + "_")
+    if args.dtype and args.dtype != W["dtype"]:
+        W["dtype"] = args.dtype
+        W["name"] = W["name"].replace("_fp32_", "_bf16_" if args.dtype == "bfloat16" else "_" + args.dtype + "_")
     if args.bytes_per_rank:
         W["bytes_per_rank"] = args.bytes_per_rank
         W["name"] += f" (profiling size {args.bytes_per_rank} B/rank)"
@@ -562,7 +654,7 @@ def main() -> int:
         total, off, count = shard_of(v, count, dtype, world, rank)
         shard = {"global_count_per_rank": total, "offset": off, "count": count}
     x = make_inputs(n, block if coll == "all_gather" else count, dtype, "uniform", seed=rank_seed(rank))
-    send = torch.from_numpy(x).cuda()
+    send = torch.from_numpy(_host(x)).cuda()
     recv = torch.empty((n, block) if coll == "reduce_scatter" else (n, count), dtype=send.dtype, device=send.device)
     sp, rp = [send[r] for r in range(n)], [recv[r] for r in range(n)]
     comm = v.vrcclCommInit(n, W["max_channels"])
@@ -621,7 +713,8 @@ def main() -> int:
     mean_kern_s = statistics.mean(kern_ms) / 1e3
     peak, peak_kind = measured_peak()
     achieved = algo_bytes / mean_kern_s / 1e9
-    traffic = profiled_traffic(S) if coll == "allreduce" and not args.direct and W["algo"] == "ring" else None
+    traffic = (profiled_traffic(S) if coll == "allreduce" and not args.direct and W["algo"] == "ring"
+               and W["proto"] == "simple" and dtype == "float32" else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
@@ -680,7 +773,7 @@ def main() -> int:
     line = {
         "metric": COLL_METRIC[coll], "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": {"float32": "f32", "bfloat16": "bf16"}[dtype], "data": "synthetic",
         "config": {"workload": W["name"], "coll": coll, "nranks": n, "bytes_per_rank": S, "count": count,
                    "op": W["op"],
                    "algo": sched["algo"], "proto": sched["proto"], "channels": sched["nchannels"],
