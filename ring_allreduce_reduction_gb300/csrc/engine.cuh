@@ -39,7 +39,9 @@ struct Agent {
   int re[2], se[2];
   unsigned long long rstep[2], sstep[2];
   int slices;     // FIFO steps done in this launch (fault injection clock)
+  int rvDone;     // receiving steps done in this launch
   bool faulty;    // this agent is the injected fault
+  unsigned long long headSeen[2];  // LL128: last value seen of each out-edge's head (per warp)
   int dre, dse;   // direct edges (ring, Simple): in and out, -1 if none
   unsigned long long drstep, dsstep;
 
@@ -49,6 +51,8 @@ struct Agent {
     ch = ch_;
     nrecv = nsend = 0;
     slices = 0;
+    rvDone = 0;
+    headSeen[0] = headSeen[1] = 0;
     dre = dse = -1;
     drstep = dsstep = 0;
     faulty = (c.faultRank == rank_ && c.faultChannel == ch_);
@@ -78,8 +82,10 @@ struct Agent {
     return c.fifo[proto] + (size_t(e) * kSteps + size_t(step % kSteps)) * slotBufferBytes(proto);
   }
   __device__ __forceinline__ void advance(int flags) {
-    if (flags & F_RECV)
+    if (flags & F_RECV) {
       for (int i = 0; i < nrecv; ++i) ++rstep[i];
+      ++rvDone;
+    }
     if (flags & F_SEND)
       for (int i = 0; i < nsend; ++i) ++sstep[i];
     ++slices;
@@ -96,27 +102,65 @@ struct Agent {
   }
 };
 
-// Thread 0 waits until every out-edge slot of this step is drained (and,
-// for Simple, every in-edge slot is filled); the CTA then learns the
-// outcome through shared memory. false = give up (abort/timeout/fault).
-__device__ __forceinline__ bool slicePrologue(const DevComm& c, Agent& ag, int flags, bool waitTail, int* smFail) {
-  if (threadIdx.x == 0) {
-    bool ok = !ag.faultNow(c);
-    if (ok && (flags & F_SEND)) {
-      for (int i = 0; i < ag.nsend && ok; ++i) {
-        unsigned long long need = ag.sstep[i] + 1;
-        if (need > (unsigned long long)kSteps)
-          ok = waitGE(&c.ctrl[ag.proto][ag.se[i]].head, need - kSteps, c, ag.rank, ag.ch, 1);
-      }
-    }
-    if (ok && waitTail && (flags & F_RECV)) {
-      for (int i = 0; i < ag.nrecv && ok; ++i)
-        ok = waitGE(&c.ctrl[ag.proto][ag.re[i]].tail, ag.rstep[i] + 1, c, ag.rank, ag.ch, 0);
-    }
-    *smFail = ok ? 0 : 1;
+// Wait (bounded) until *p >= need, acquiring it, with a cached last-seen
+// value that spares the poll when it already covers `need`.
+__device__ __forceinline__ bool flagAtLeast(const DevComm& c, const Agent& ag, const unsigned long long* p,
+                                            unsigned long long need, unsigned long long& seen, int kind) {
+  if (seen >= need) return true;
+  Spin sp;
+  unsigned long long v;
+  while ((v = ldAcquire(p)) < need) {
+    if (sp.tick(c, ag.rank, ag.ch, kind, need)) return false;
   }
+  seen = v;
+  return true;
+}
+
+// LL128: per FIFO slot, the warps of the agent that are done reading it;
+// monotonic within a launch (zeroed at its start by llBegin).
+__device__ __forceinline__ unsigned* llSlotDone() {
+  __shared__ unsigned cnt[kSteps];
+  return cnt;
+}
+__device__ __forceinline__ void llBegin() {
+  if (threadIdx.x < kSteps) llSlotDone()[threadIdx.x] = 0;
   __syncthreads();
-  return *smFail == 0;
+}
+
+// LL / LL128, per warp: wait until every out-edge slot of this step is
+// drained (lane 0 polls each head, caching the value it saw); false = give
+// up (abort/timeout/fault).
+__device__ __forceinline__ bool warpCredit(const DevComm& c, Agent& ag, int flags, int proto) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    ok = !ag.faultNow(c);
+    if (ok && (flags & F_SEND))
+      for (int i = 0; i < ag.nsend && ok; ++i) {
+        const unsigned long long need = ag.sstep[i] + 1;
+        if (need > (unsigned long long)kSteps)
+          ok = flagAtLeast(c, ag, &c.ctrl[proto][ag.se[i]].head, need - kSteps, ag.headSeen[i], 1);
+      }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// LL / LL128, per warp, after its reads of a received slice: the last warp
+// of the agent done with it returns the slot(s) to the sender. A warp runs
+// ahead of another by fewer than VRCCL_STEPS receiving steps (reading a
+// slot's next use needs the sender to have seen it returned), so one
+// counter per slot, growing within the launch, tells when a use is done.
+// The count is a relaxed shared-memory atomic: a warp counts itself only
+// after it has used every value it loaded from the slot, so its loads are
+// done (an acquire-release atomic here made every step wait for the warp's
+// stores to complete: 8-byte calls 12.5 -> 14.9 us).
+__device__ __forceinline__ void warpDoneReading(const DevComm& c, Agent& ag, int proto, int lane) {
+  __syncwarp();  // every lane's loads of the slot are done
+  if (lane == 0) {
+    const unsigned k = unsigned(ag.rvDone);
+    const unsigned prev = atomicAdd(&llSlotDone()[k % kSteps], 1u);
+    if (prev + 1 == (k / kSteps + 1) * unsigned(blockDim.x >> 5))
+      for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[proto][ag.re[i]].head, ag.rstep[i] + 1);
+  }
 }
 
 // Reduction of one group of NW 32-bit words.
@@ -221,9 +265,9 @@ __device__ __forceinline__ void storeUnit(char* p, uint2 v, int validBytes) {
 template <int DT, int OP, bool TREE, class Args>
 __device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
   using S = typename Ty<DT>::S;
-  __shared__ int smFail;
   const DevComm& c = a.comm;
-  if (!slicePrologue(c, ag, flags, false, &smFail)) return false;
+  const int lane = threadIdx.x & 31;
+  if (!warpCredit(c, ag, flags, kLL)) return false;
 
   const int nbytes = nelem * int(sizeof(S));
   const int nu = (nbytes + 7) / 8;
@@ -272,11 +316,8 @@ __device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int
       for (int i = 0; i < ag.nsend; ++i) stVolatile16(dst[i] + u, make_uint4(acc[0], sflag[i], acc[1], sflag[i]));
     if (flags & F_OUT) storeUnit<S>(out + 8 * u, make_uint2(acc[0], acc[1]), valid);
   }
-  if (fail) smFail = 1;
-  __syncthreads();
-  if (smFail) return false;
-  if (threadIdx.x == 0 && rv)
-    for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[kLL][ag.re[i]].head, ag.rstep[i] + 1);
+  if (__any_sync(0xffffffffu, fail)) return false;
+  if (rv) warpDoneReading(c, ag, kLL, lane);
   ag.advance(flags);
   return true;
 }
@@ -298,6 +339,13 @@ __device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int
 // volatile and L2-only accesses, writer and reader on the same and on
 // different dies: no torn 16-byte piece, no torn 128-byte line); the GPU
 // tests stress it.
+// a ? x : y as one selp (no branch on a per-lane condition)
+__device__ __forceinline__ uint32_t selectWord(bool a, uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("{\n.reg .pred q;\nsetp.ne.u32 q, %1, 0;\nselp.b32 %0, %2, %3, q;\n}" : "=r"(r) : "r"(uint32_t(a)), "r"(x), "r"(y));
+  return r;
+}
+
 template <int U, int DT, int OP, bool TREE, class Args>
 __device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char* in, char* out, int nbytes,
                                             int nlines, int flags, const char* const* src, char* const* dst) {
@@ -352,6 +400,8 @@ __device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char
           bool all = true;
 #pragma unroll
           for (int u = 0; u < U; ++u) {
+            // the eight lanes of a line load it together, in one instruction
+            __syncwarp();
             uint4 v = make_uint4(0, 0, 0, 0);
             if (!have[u]) v = ldVolatile16(reinterpret_cast<const uint4*>(src[i] + size_t(g0 + 4 * u + k) * 128 + p * 16));
             const bool flagOk = p == 7 && v.z == wlo && v.w == whi;
@@ -378,15 +428,22 @@ __device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char
     for (int u = 0; u < U; ++u)
       reduceWords<DT, OP, TREE, 4>(acc[u], x[u], r[u][0], r[u][NR - 1], flags, ag.nrecv, a.scale, a.nranks);
     if (flags & F_SEND) {
-      // one warp store per group of four lines, the flag in lane 7's piece
+      // One warp store per group of four lines, the flag in lane 7's piece.
+      // A line must leave in one instruction of its eight lanes: the words
+      // are chosen without a branch (a branch on the lane could let the
+      // compiler issue the flag lane's store apart from the others'), and
+      // the warp is brought together right before each store.
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (g0 + 4 * u + k >= nlines) continue;
+        const bool active = g0 + 4 * u + k < nlines;
         for (int i = 0; i < ag.nsend; ++i) {
           const unsigned long long f = ag.sstep[i] + 1;
-          const uint4 piece = p < 7 ? make_uint4(acc[u][0], acc[u][1], acc[u][2], acc[u][3])
-                                    : make_uint4(acc[u][0], acc[u][1], uint32_t(f), uint32_t(f >> 32));
-          stVolatile16(reinterpret_cast<uint4*>(dst[i] + size_t(g0 + 4 * u + k) * 128 + p * 16), piece);
+          const uint32_t w2 = selectWord(p < 7, acc[u][2], uint32_t(f));
+          const uint32_t w3 = selectWord(p < 7, acc[u][3], uint32_t(f >> 32));
+          __syncwarp();
+          if (active)
+            stVolatile16(reinterpret_cast<uint4*>(dst[i] + size_t(g0 + 4 * u + k) * 128 + p * 16),
+                         make_uint4(acc[u][0], acc[u][1], w2, w3));
         }
       }
     }
@@ -401,12 +458,18 @@ __device__ __forceinline__ bool ll128Passes(const Args& a, Agent& ag, const char
   return !fail;
 }
 
+// One LL128 slice. Every warp works on its own: it waits for the out-edges'
+// credit itself (lane 0 polls the head, caching it), and the last warp
+// done reading the slice returns the slot(s) to the sender; no CTA-wide
+// barrier per slice. A warp can run ahead of another by fewer than
+// VRCCL_STEPS slices (reading a slot's next use needs the sender to have
+// seen the slot returned), so one counter per slot tells when a use is done.
 template <int U, int DT, int OP, bool TREE, class Args>
 __device__ bool llSlice128(const Args& a, Agent& ag, const char* in, char* out, int nelem, int flags) {
   using S = typename Ty<DT>::S;
-  __shared__ int smFail;
   const DevComm& c = a.comm;
-  if (!slicePrologue(c, ag, flags, false, &smFail)) return false;
+  const int lane = threadIdx.x & 31;
+  if (!warpCredit(c, ag, flags, kLL128)) return false;
   const int nbytes = nelem * int(sizeof(S));
   const int nlines = (nbytes + kLL128DataBytes - 1) / kLL128DataBytes;
   const bool rv = (flags & F_RECV) && ag.nrecv > 0;
@@ -420,12 +483,8 @@ __device__ bool llSlice128(const Args& a, Agent& ag, const char* in, char* out, 
   // flight per warp; U = 1: the shortest chain per line. The two live in
   // different kernels: the four-group code in the same kernel measured
   // slower on short slices (ring LL128, bf16 16 KiB: 37 -> 49 us).
-  const bool ok = ll128Passes<U, DT, OP, TREE>(a, ag, in, out, nbytes, nlines, flags, src, dst);
-  if (!ok && (threadIdx.x & 31) == 0) smFail = 1;
-  __syncthreads();
-  if (smFail) return false;
-  if (threadIdx.x == 0 && rv)
-    for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[kLL128][ag.re[i]].head, ag.rstep[i] + 1);
+  if (!ll128Passes<U, DT, OP, TREE>(a, ag, in, out, nbytes, nlines, flags, src, dst)) return false;
+  if (rv) warpDoneReading(c, ag, kLL128, lane);
   ag.advance(flags);
   return true;
 }

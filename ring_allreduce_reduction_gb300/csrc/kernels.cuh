@@ -43,6 +43,7 @@ __device__ __forceinline__ void ringAgent(const Args& a, Agent& ag, It& it, cons
   if constexpr (PROTO == kSimple) {
     simplePipeline<DT, OP, false, DIRECT>(a, ag, it, in, out);
   } else {
+    llBegin();
     SliceDesc d;
     while (it.next(d))
       if (!runSlice<PROTO, DT, OP, false>(a, ag, in + d.inPos * E, out + d.outPos * E, d.nelem, d.flags)) return;
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) treeKernel(const __gri
   if constexpr (PROTO == kSimple) {
     simplePipeline<DT, OP, true>(a, ag, it, in, out);
   } else {
+    llBegin();
     SliceDesc d;
     while (it.next(d))
       if (!runSlice<PROTO, DT, OP, true>(a, ag, in + d.inPos * E, out + d.outPos * E, d.nelem, d.flags)) return;

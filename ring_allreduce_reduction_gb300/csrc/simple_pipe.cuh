@@ -50,19 +50,6 @@ __device__ __forceinline__ bool pipeWait(const DevComm& c, const Agent& ag, Pipe
   return true;
 }
 
-// Producer side of a flag wait with a cached last-seen value.
-__device__ __forceinline__ bool flagAtLeast(const DevComm& c, const Agent& ag, const unsigned long long* p,
-                                            unsigned long long need, unsigned long long& seen, int kind) {
-  if (seen >= need) return true;
-  Spin sp;
-  unsigned long long v;
-  while ((v = ldAcquire(p)) < need) {
-    if (sp.tick(c, ag.rank, ag.ch, kind, need)) return false;
-  }
-  seen = v;
-  return true;
-}
-
 // Waits (bounded) until every bulk copy this thread issued into the stage
 // ring has landed; a CTA must not exit with copies into its shared memory in
 // flight.

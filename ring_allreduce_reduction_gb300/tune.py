@@ -31,7 +31,8 @@ import time
 import torch
 
 ELEM = {"int32": 4, "float32": 4, "bfloat16": 2, "float16": 2, "int8": 1, "uint8": 1, "int64": 8, "float64": 8}
-TORCH = {"int32": torch.int32, "float32": torch.float32, "bfloat16": torch.bfloat16, "float16": torch.float16}
+TORCH = {"int32": torch.int32, "float32": torch.float32, "bfloat16": torch.bfloat16, "float16": torch.float16,
+         "int8": torch.int8, "uint8": torch.uint8, "int64": torch.int64, "float64": torch.float64}
 
 
 def time_call(v, comm, sp, rp, count, dtype, op, algo, proto, iters, warmup, stream) -> float:
@@ -80,7 +81,10 @@ def sweep(nranks: int, dtype: str, sizes: list[int], protos: list[str], algos: l
     maxcount = max(sizes) // E
     pad = (maxcount + 15) // 16 * 16
     send = torch.zeros((nranks, pad), dtype=TORCH[dtype], device="cuda")
-    send.uniform_(-1, 1) if dtype != "int32" else send.random_(-1000, 1000)
+    if dtype in ("int32", "int8", "uint8", "int64"):
+        send.random_(0, 100)
+    else:
+        send.uniform_(-1, 1)
     recv = torch.empty_like(send)
     sp = [send[r] for r in range(nranks)]
     rp = [recv[r] for r in range(nranks)]
