@@ -145,22 +145,38 @@ __device__ __forceinline__ bool warpCredit(const DevComm& c, Agent& ag, int flag
 }
 
 // LL / LL128, per warp, after its reads of a received slice: the last warp
-// of the agent done with it returns the slot(s) to the sender. A warp runs
-// ahead of another by fewer than VRCCL_STEPS receiving steps (reading a
-// slot's next use needs the sender to have seen it returned), so one
-// counter per slot, growing within the launch, tells when a use is done.
+// of the agent done with it returns the slot(s) to the sender. One
+// shared-memory counter per slot position, growing within the launch,
+// counts the warps done with each use; before counting itself for receiving
+// step k a warp waits (bounded) until every warp has counted step k -
+// VRCCL_STEPS, the counter's previous use. (A warp with no lines in a
+// slice waits for no flag, so without that wait it could run a whole
+// counter cycle ahead of a slower warp and the counts of two uses would
+// mix: a grouped run of small tasks did that and never returned a slot.)
 // The count is a relaxed shared-memory atomic: a warp counts itself only
 // after it has used every value it loaded from the slot, so its loads are
 // done (an acquire-release atomic here made every step wait for the warp's
-// stores to complete: 8-byte calls 12.5 -> 14.9 us).
-__device__ __forceinline__ void warpDoneReading(const DevComm& c, Agent& ag, int proto, int lane) {
+// stores to complete). false = gave up (abort/timeout).
+__device__ __forceinline__ bool warpDoneReading(const DevComm& c, Agent& ag, int proto, int lane) {
   __syncwarp();  // every lane's loads of the slot are done
+  int ok = 1;
   if (lane == 0) {
     const unsigned k = unsigned(ag.rvDone);
-    const unsigned prev = atomicAdd(&llSlotDone()[k % kSteps], 1u);
-    if (prev + 1 == (k / kSteps + 1) * unsigned(blockDim.x >> 5))
-      for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[proto][ag.re[i]].head, ag.rstep[i] + 1);
+    const unsigned W = blockDim.x >> 5;
+    unsigned* cnt = &llSlotDone()[k % kSteps];
+    Spin sp(15u);
+    while (*reinterpret_cast<volatile unsigned*>(cnt) < (k / kSteps) * W)
+      if (sp.tick(c, ag.rank, ag.ch, 4, ag.rstep[0] + 1)) {
+        ok = 0;
+        break;
+      }
+    if (ok) {
+      const unsigned prev = atomicAdd(cnt, 1u);
+      if (prev + 1 == (k / kSteps + 1) * W)
+        for (int i = 0; i < ag.nrecv; ++i) stRelaxed(&c.ctrl[proto][ag.re[i]].head, ag.rstep[i] + 1);
+    }
   }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Reduction of one group of NW 32-bit words.
@@ -317,7 +333,7 @@ __device__ bool llSlice(const Args& a, Agent& ag, const char* in, char* out, int
     if (flags & F_OUT) storeUnit<S>(out + 8 * u, make_uint2(acc[0], acc[1]), valid);
   }
   if (__any_sync(0xffffffffu, fail)) return false;
-  if (rv) warpDoneReading(c, ag, kLL, lane);
+  if (rv && !warpDoneReading(c, ag, kLL, lane)) return false;
   ag.advance(flags);
   return true;
 }
@@ -484,7 +500,7 @@ __device__ bool llSlice128(const Args& a, Agent& ag, const char* in, char* out, 
   // different kernels: the four-group code in the same kernel measured
   // slower on short slices (ring LL128, bf16 16 KiB: 37 -> 49 us).
   if (!ll128Passes<U, DT, OP, TREE>(a, ag, in, out, nbytes, nlines, flags, src, dst)) return false;
-  if (rv) warpDoneReading(c, ag, kLL128, lane);
+  if (rv && !warpDoneReading(c, ag, kLL128, lane)) return false;
   ag.advance(flags);
   return true;
 }

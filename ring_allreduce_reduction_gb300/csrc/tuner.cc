@@ -31,6 +31,26 @@ static int log2Bucket(size_t bytes) {
 
 Choice Tuner::choose(int nranks, size_t bytes, int esize, int maxChannels, unsigned algoMask,
                      unsigned protoMask) const {
+  // the choice depends on the size only through its bucket (nearest power
+  // of two) and the size rule's thresholds; key on both
+  const int bucket = log2Bucket(bytes);
+  const int rule = bytes <= 65536 ? 0 : bytes <= (size_t(2) << 20) ? 1 : 2;
+  const uint64_t key = (uint64_t(nranks) << 48) ^ (uint64_t(bucket) << 40) ^ (uint64_t(rule) << 38) ^
+                       (uint64_t(esize & 15) << 34) ^ (uint64_t(maxChannels & 127) << 24) ^
+                       (uint64_t(algoMask & 255) << 8) ^ uint64_t(protoMask & 255);
+  {
+    std::lock_guard<std::mutex> lk(mu_);
+    auto it = memo_.find(key);
+    if (it != memo_.end()) return it->second;
+  }
+  const Choice c = scan(nranks, bytes, esize, maxChannels, algoMask, protoMask);
+  std::lock_guard<std::mutex> lk(mu_);
+  memo_.emplace(key, c);
+  return c;
+}
+
+Choice Tuner::scan(int nranks, size_t bytes, int esize, int maxChannels, unsigned algoMask,
+                   unsigned protoMask) const {
   // the size rule's preference order, first allowed protocol wins
   static const int kSmall[3] = {kLL, kLL128, kSimple}, kMid[3] = {kLL128, kSimple, kLL},
                    kLarge[3] = {kSimple, kLL128, kLL};
@@ -108,6 +128,7 @@ int Tuner::load(const char* path, int nranks) {
     }
   }
   fclose(f);
+  forget();
   return count;
 }
 

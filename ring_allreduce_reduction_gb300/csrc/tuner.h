@@ -15,7 +15,10 @@
 #pragma once
 
 #include <cstddef>
+#include <cstdint>
+#include <mutex>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 namespace vrccl {
@@ -58,12 +61,36 @@ class Tuner {
   // the element size applies to every element type.
   void loadEnvFile(int nranks);
   int load(const char* path, int nranks);  // entries read, -1 on error
-  void add(const Entry& e) { table_.push_back(e); }
-  void clear() { table_.clear(); }
+  void add(const Entry& e) {
+    table_.push_back(e);
+    forget();
+  }
+  void clear() {
+    table_.clear();
+    forget();
+  }
   size_t size() const { return table_.size(); }
+  Tuner() = default;
+  Tuner(const Tuner& o) : table_(o.table_) {}
+  Tuner& operator=(const Tuner& o) {
+    table_ = o.table_;
+    forget();
+    return *this;
+  }
 
  private:
+  Choice scan(int nranks, size_t bytes, int esize, int maxChannels, unsigned algoMask, unsigned protoMask) const;
+  void forget() {
+    std::lock_guard<std::mutex> lk(mu_);
+    memo_.clear();
+  }
   std::vector<Entry> table_;
+  // A call's choice depends only on (rank count, power-of-two size bucket,
+  // element size, channel budget, masks); it is found by a scan of the
+  // table once and kept, so a call does no search (the tables hold
+  // thousands of rows).
+  mutable std::mutex mu_;
+  mutable std::unordered_map<uint64_t, Choice> memo_;
 };
 
 }  // namespace vrccl

@@ -67,7 +67,7 @@ def test_shipped_tables_drive_auto(v, n, monkeypatch, capfd):
     monkeypatch.setenv("VRCCL_DEBUG", "INFO")
     comm = v.vrcclCommInit(n, 64)
     try:
-        for count in (64, 1 << 14, 1 << 17):
+        for count in (64, 1 << 14, 1 << 17, 64, 70):  # repeated and same-bucket sizes: the kept choices
             x = make_inputs(n, count, "float32", "normal", seed=4)
             y, sched, _ = run(v, comm, x, "float32", "sum", "auto", "auto")
             want = tune.table_choice(rows, n, count * 4, 4)
@@ -75,7 +75,7 @@ def test_shipped_tables_drive_auto(v, n, monkeypatch, capfd):
             _check(x, y, sched)
         err = capfd.readouterr().err
         lines = [ln for ln in err.splitlines() if "VRCCL INFO AllReduce" in ln]
-        assert len(lines) == 3 and all("tuning measured (4-byte rows" in ln for ln in lines), lines
+        assert len(lines) == 5 and all("tuning measured (4-byte rows" in ln for ln in lines), lines
     finally:
         v.vrcclCommDestroy(comm)
 
