@@ -452,8 +452,12 @@ vrcclResult_t vrcclCommGetLaunchShape(vrcclComm_t comm, int* blocks, int* thread
  * time T = lat + bytes/bw [Architecture §8.2]; this table holds measured
  * times instead, and algo/proto/channels "auto" take its minimum at the
  * nearest measured power-of-two size. File format, one entry per line:
- *   nranks algo proto channels log2bytes sliceBytes microseconds
- * ('#' starts a comment; algo/proto use the enum values above).
+ *   nranks algo proto channels log2bytes sliceBytes microseconds [elementBytes]
+ * ('#' starts a comment; algo/proto use the enum values above). A line with
+ * elementBytes (1, 2, 4 or 8) applies to calls whose element type has that
+ * size; a line without it applies to every element type. A call takes the
+ * rows of its own element size if the table has any, else the rows without
+ * one, else those of the nearest element size (the larger on a tie).
  *   loaded  out (may be NULL): entries kept.
  * Errors: vrcclInvalidArgument (null comm/path, unreadable file).
  */

@@ -11,7 +11,8 @@ run of the flag protocols.
   association predictor.
 * LL and LL128 stress: many launches of random sizes and channel counts at
   n = 8 and n = 72 on one communicator, so the flags run on across launches
-  (each line is written with one 16-byte store carrying data and flags; a
+  (an LL line is one 16-byte store carrying data and flags, an LL128 line
+  one warp store of eight 16-byte pieces with the flag in the last; a
   reader that saw a torn line would show up here as a wrong bit).
 """
 import numpy as np
