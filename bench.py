@@ -595,14 +595,17 @@ def main() -> int:
     ap.add_argument("--algo", default="ring", choices=["ring", "tree", "oneshot"],
                     help="allreduce only: the schedule timed (the workload's is the ring)")
     ap.add_argument("--no-bound", action="store_true", help="skip timing the one-shot bound beside the ring")
-    ap.add_argument("--direct", action="store_true",
-                    help="ring AllReduce with the direct all-gather (through the recv buffers)")
+    ap.add_argument("--fifo", action="store_true",
+                    help="ring AllReduce with its all-gather through the FIFOs (the library's default runs it "
+                         "through the recv buffers)")
     ap.add_argument("--bucket", default="", choices=["", "flat", "group", "separate"],
                     help="time the 224-tensor bf16 gradient bucket instead of the workload")
     ap.add_argument("--proto", default="", choices=["", "simple", "ll", "ll128"],
                     help="profiling only: another protocol than the workload's (named in config)")
     ap.add_argument("--dtype", default="", choices=["", "float32", "bfloat16"],
                     help="profiling only: another element type than the workload's (named in config)")
+    ap.add_argument("--op", default="", choices=["", "sum", "prod", "max", "min", "avg"],
+                    help="profiling only: another reduction op than the workload's (named in config)")
     ap.add_argument("--bytes-per-rank", type=int, default=0,
                     help="profiling only: a smaller per-rank size than the workload's (reported in config)")
     args = ap.parse_args()
@@ -640,6 +643,9 @@ def main() -> int:
     if args.dtype and args.dtype != W["dtype"]:
         W["dtype"] = args.dtype
         W["name"] = W["name"].replace("_fp32_", "_bf16_" if args.dtype == "bfloat16" else "_" + args.dtype + "_")
+    if args.op and args.op != W["op"]:
+        W["name"] = W["name"].replace("_" + W["op"] + "_", "_" + args.op + "_")
+        W["op"] = args.op
     if args.bytes_per_rank:
         W["bytes_per_rank"] = args.bytes_per_rank
         W["name"] += f" (profiling size {args.bytes_per_rank} B/rank)"
@@ -658,9 +664,9 @@ def main() -> int:
     recv = torch.empty((n, block) if coll == "reduce_scatter" else (n, count), dtype=send.dtype, device=send.device)
     sp, rp = [send[r] for r in range(n)], [recv[r] for r in range(n)]
     comm = v.vrcclCommInit(n, W["max_channels"])
-    if args.direct:
-        v.vrcclCommSetDirect(comm, True)
-        W["name"] += "_direct"
+    if args.fifo:
+        v.vrcclCommSetDirect(comm, False)
+        W["name"] += "_fifo"
     stream = torch.cuda.current_stream()
 
     def step():
@@ -713,7 +719,7 @@ def main() -> int:
     mean_kern_s = statistics.mean(kern_ms) / 1e3
     peak, peak_kind = measured_peak()
     achieved = algo_bytes / mean_kern_s / 1e9
-    traffic = (profiled_traffic(S) if coll == "allreduce" and not args.direct and W["algo"] == "ring"
+    traffic = (profiled_traffic(S) if coll == "allreduce" and not args.fifo and W["algo"] == "ring"
                and W["proto"] == "simple" and dtype == "float32" else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,

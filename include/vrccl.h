@@ -25,7 +25,9 @@
  * chunked as RingARAlgorithm::getNextSendAddr describes [Deep Dive §2.3;
  * Architecture §9.4, runRing]; rank r hands chunks to rank r+1 (mod n)
  * through staging FIFOs in global memory, synchronised by one of the three
- * wire protocols Simple, LL and LL128 [Architecture §7.2]. The tree
+ * wire protocols Simple, LL and LL128 [Architecture §7.2]; with Simple the
+ * all-gather writes each finished chunk straight into the next rank's recv
+ * buffer instead (runRing's direct primitives; vrcclCommSetDirect). The tree
  * algorithm reduces up and broadcasts down the double binary tree
  * [Architecture §5.4, §9.4; Deep Dive ch.4, ncclGetBtree/ncclGetDtree].
  *
@@ -168,8 +170,8 @@ typedef enum {
  * VRCCL_SLICE_BYTES (largest Simple FIFO slot to use, bytes; default and
  * most 32768), VRCCL_SIMPLE_WARPS (most consumer warps per Simple agent, at
  * most 16; default 16 for 2-byte types, 8 for 4-byte ones), VRCCL_PREFETCH (input slices a Simple agent pulls into L2
- * ahead of use, default 0 = off, at most 32), VRCCL_DIRECT (1: see
- * vrcclCommSetDirect), VRCCL_TUNE_FILE (a measured
+ * ahead of use, default 0 = off, at most 32), VRCCL_DIRECT (default 1; 0
+ * selects the FIFO all-gather, see vrcclCommSetDirect), VRCCL_TUNE_FILE (a measured
  * tuning table, see vrcclCommLoadTuning; without it the table shipped next
  * to the library, tuning/gb300_n<nranks>.txt, is used when present).
  */
@@ -346,18 +348,19 @@ vrcclResult_t vrcclModelPredict(const vrcclModelGraph_t* graph, vrcclAlgo_t algo
                                 int numPipeOps, float* latUs, float* algBwGBs, float* timeUs);
 
 /*
- * vrcclCommSetDirect -- 1: the communicator's later ring / Simple
- * AllReduces run the all-gather through the ranks' recv buffers instead of
- * the FIFOs (the directRecvCopyDirectSend primitives of runRing, which
+ * vrcclCommSetDirect -- 1 (the default): the communicator's later ring /
+ * Simple AllReduces run the all-gather through the ranks' recv buffers
+ * instead of the FIFOs (the directRecvCopyDirectSend primitives of runRing, which
  * read and write a peer's user buffer where the ranks can address each
  * other, [Architecture §9.4, §10]): the step that finishes chunk r writes
  * it to rank r's recv buffer and straight into rank r+1's, each later step
  * forwards it from the rank's own recv buffer into the next rank's, and a
  * counter per ring edge, released after the writes, tells the next rank it
  * is there. The reduce-scatter still moves through the FIFOs. Results are
- * bit-identical to the FIFO form. 0 (the default, or VRCCL_DIRECT unset /
- * 0 at vrcclCommInit) restores the FIFO all-gather. LL, LL128, the tree,
- * the phases run alone and grouped launches always use the FIFOs.
+ * bit-identical to the FIFO form, which moves (6n-4) S bytes through the
+ * SMs against the direct form's (5n-4) S. 0 (or VRCCL_DIRECT=0 at
+ * vrcclCommInit) selects the FIFO all-gather. LL, LL128, the tree, the
+ * phases run alone and grouped launches always use the FIFOs.
  * Errors: vrcclInvalidArgument (bad handle, enable not 0 or 1).
  */
 vrcclResult_t vrcclCommSetDirect(vrcclComm_t comm, int enable);

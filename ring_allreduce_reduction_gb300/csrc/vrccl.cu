@@ -263,7 +263,7 @@ extern "C" vrcclResult_t vrcclCommInit(vrcclComm_t* comm, int nranks, int nchann
   c->envSliceBytes = (size_t)std::max(0, envInt("VRCCL_SLICE_BYTES", 0)) / 16 * 16;
   c->envWarps = std::max(0, envInt("VRCCL_SIMPLE_WARPS", 0));
   c->envPrefetch = std::min(kMaxPrefetch, std::max(0, envInt("VRCCL_PREFETCH", 0)));
-  c->direct = envInt("VRCCL_DIRECT", 0) != 0;
+  c->direct = envInt("VRCCL_DIRECT", 1) != 0;
   c->tuner.loadEnvFile(nranks);
   {
     std::lock_guard<std::mutex> lk(gLiveMu);
@@ -576,10 +576,12 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
     const int nbuf = A == kTree ? 3 : 2;
     SimpleShape sh;
     // 2-byte types do twice the element arithmetic per byte: with a large
-    // share per agent their consumers need twice the warps to keep up
-    // (measured on the bf16 avg bucket: 8 warps 6.2 ms, 16 warps 5.1 ms;
-    // fp32 is 2 % slower with 16). Below 1 MiB per agent the larger block
-    // only adds latency (bf16 1 KiB: 41 us with 8 warps, 49 us with 16).
+    // share per agent they take twice the consumer warps (measured on the
+    // bf16 avg bucket, 1 GiB per rank: 16 warps 3.57 ms, 8 warps 3.61 ms;
+    // before the ring's consumer loop was compiled per slice kind 5.1 and
+    // 6.2 ms; the bf16 sum at 256 MiB is 3 % faster with 8, fp32 2 %
+    // slower with 16). Below 1 MiB per agent the larger block only adds
+    // latency (bf16 1 KiB: 41 us with 8 warps, 49 us with 16).
     const bool wide = kE == 2 && bytes / std::max(C, 1) >= (size_t(1) << 20);
     const int maxWarps = comm->envWarps ? std::min(comm->envWarps, kMaxConsumerWarps) : (wide ? 16 : 8);
     while (!pickSimpleShape(comm, fn, per * C, nbuf, wantSlice, maxWarps, &sh)) {

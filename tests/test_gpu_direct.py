@@ -1,8 +1,8 @@
-"""GPU parity of the direct all-gather (vrcclCommSetDirect): the ring /
-Simple AllReduce whose all-gather moves through the ranks' recv buffers
-must give the oracle's bits, and the FIFO form's, for every type, op, rank
-count, ragged end and in place; switching between the two forms on one
-communicator must keep both correct."""
+"""GPU parity of the two all-gather forms of the ring / Simple AllReduce
+(vrcclCommSetDirect): through the ranks' recv buffers (the default) and
+through the FIFOs. Both must give the oracle's bits for every type, op,
+rank count, ragged end and in place; switching between the two forms on
+one communicator must keep both correct."""
 import numpy as np
 import pytest
 
@@ -41,14 +41,15 @@ def _same(a, b):
     return np.array_equal(np.ascontiguousarray(a).view(np.uint8), np.ascontiguousarray(b).view(np.uint8))
 
 
+@pytest.mark.parametrize("direct", [True, False])
 @pytest.mark.parametrize("n", [2, 3, 5, 8])
-def test_direct_every_dtype_and_op(v, n):
+def test_direct_every_dtype_and_op(v, n, direct):
     """3 channels, 256-byte chunks: several loops, a short last loop, a
-    ragged end shorter than 16 bytes."""
+    ragged end shorter than 16 bytes; both all-gather forms."""
     comm = v.vrcclCommInit(n, 4)
     try:
         v.vrcclCommSetSchedule(comm, 3, 256)
-        v.vrcclCommSetDirect(comm, True)
+        v.vrcclCommSetDirect(comm, direct)
         for dtype in DT:
             count = COUNT[ELEM_SIZE[dtype]]
             for op in OPS:
@@ -129,6 +130,7 @@ def test_direct_full_size_matches_fifo_form(v):
     r2 = torch.empty_like(send)
     comm = v.vrcclCommInit(n, 32)
     try:
+        v.vrcclCommSetDirect(comm, False)
         v.vrcclAllReduce([send[r] for r in range(n)], [r1[r] for r in range(n)], count, "float32", "sum", "ring",
                          "simple", comm)
         s1 = v.vrcclCommGetLastSchedule(comm)
