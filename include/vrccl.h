@@ -349,8 +349,8 @@ vrcclResult_t vrcclModelPredict(const vrcclModelGraph_t* graph, vrcclAlgo_t algo
 
 /*
  * vrcclCommSetDirect -- 1 (the default): the communicator's later ring /
- * Simple AllReduces run the all-gather through the ranks' recv buffers
- * instead of the FIFOs (the directRecvCopyDirectSend primitives of runRing, which
+ * Simple AllReduces and AllGathers run the all-gather through the ranks'
+ * recv buffers instead of the FIFOs (the directRecvCopyDirectSend primitives of runRing, which
  * read and write a peer's user buffer where the ranks can address each
  * other, [Architecture §9.4, §10]): the step that finishes chunk r writes
  * it to rank r's recv buffer and straight into rank r+1's, each later step
@@ -358,9 +358,11 @@ vrcclResult_t vrcclModelPredict(const vrcclModelGraph_t* graph, vrcclAlgo_t algo
  * counter per ring edge, released after the writes, tells the next rank it
  * is there. The reduce-scatter still moves through the FIFOs. Results are
  * bit-identical to the FIFO form, which moves (6n-4) S bytes through the
- * SMs against the direct form's (5n-4) S. 0 (or VRCCL_DIRECT=0 at
- * vrcclCommInit) selects the FIFO all-gather. LL, LL128, the tree, the
- * phases run alone and grouped launches always use the FIFOs.
+ * SMs against the direct form's (5n-4) S. A standalone AllGather moves
+ * each block the same way: written into the next rank's recv buffer, then
+ * forwarded from there. 0 (or VRCCL_DIRECT=0 at vrcclCommInit) selects the
+ * FIFO all-gather. LL, LL128, the tree, ReduceScatter and grouped launches
+ * always use the FIFOs.
  * Errors: vrcclInvalidArgument (bad handle, enable not 0 or 1).
  */
 vrcclResult_t vrcclCommSetDirect(vrcclComm_t comm, int enable);

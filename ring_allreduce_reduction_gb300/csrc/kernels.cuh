@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) ringKernel(const __gri
     ag.addRecv(c, ringEdge(ch, (r - 1 + n) % n, n));
     ag.addSend(c, ringEdge(ch, r, n));
   }
-  const bool direct = PROTO == kSimple && a.direct && a.coll == kAllReduce && n > 1;
+  const bool direct = PROTO == kSimple && a.direct && (a.coll == kAllReduce || a.coll == kAllGather) && n > 1;
   if (direct) ag.addDirect(c, ringEdge(ch, (r - 1 + n) % n, n), ringEdge(ch, r, n));
   if (a.coll == kAllReduce || n == 1) {
     RingIter it;
@@ -89,8 +89,15 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) ringKernel(const __gri
   } else {
     PhaseIter it;
     it.init(n, r, a.coll == kAllGather, (long long)lo, (long long)(hi - lo), (long long)a.count, a.chunkElems,
-            a.sliceElems);
-    ringAgent<PROTO, DT, OP>(a, ag, it, in, out);
+            a.sliceElems, direct);
+    if constexpr (PROTO == kSimple) {
+      if (direct)
+        ringAgent<PROTO, DT, OP, true>(a, ag, it, in, out);
+      else
+        ringAgent<PROTO, DT, OP, false>(a, ag, it, in, out);
+    } else {
+      ringAgent<PROTO, DT, OP>(a, ag, it, in, out);
+    }
   }
 }
 

@@ -144,19 +144,27 @@ struct RingIter {
 //   AllGather      p = 0 copySend c = r (own send buffer -> block r);
 //                  p = 1..n-2 recvCopySend c = r-p; p = n-1 recv c = r+1
 // (n > 1; one rank runs the AllReduce copy instead).
+// direct (AllGather, Simple): as the ring's direct all-gather, each block
+// moves through the recv buffers: step 0 writes the own block to this
+// rank's recv buffer and into the next rank's, each later step forwards
+// the block the predecessor wrote here into the next rank's recv buffer,
+// and the last step's slices are passed over and only counted (dskip).
 struct PhaseIter {
   int n, r;
-  bool gather;
+  bool gather, direct;
   long long lo, chCount, blk, K, slice;
   long long off, len, inBase, outBase, s;
+  long long dskip;  // direct: slices of the last steps passed over so far
   int p, flags;
   bool started;
 
   __device__ __forceinline__ void init(int n_, int r_, bool gather_, long long lo_, long long chCount_,
-                                       long long blk_, long long K_, long long slice_) {
+                                       long long blk_, long long K_, long long slice_, bool direct_ = false) {
     n = n_;
     r = r_;
     gather = gather_;
+    direct = direct_ && gather_;
+    dskip = 0;
     lo = lo_;
     chCount = chCount_;
     blk = blk_;
@@ -176,11 +184,18 @@ struct PhaseIter {
       outBase = lo + off;
     } else {
       c = ((r - p) % n + n) % n;
-      flags = p == 0 ? (F_IN | F_OUT | F_SEND) : p < n - 1 ? (F_RECV | F_OUT | F_SEND) : (F_RECV | F_OUT);
+      if (direct)
+        flags = p == 0 ? (F_IN | F_OUT | F_DSEND) : (F_DRECV | F_DSEND);
+      else
+        flags = p == 0 ? (F_IN | F_OUT | F_SEND) : p < n - 1 ? (F_RECV | F_OUT | F_SEND) : (F_RECV | F_OUT);
       inBase = lo + off;
       outBase = (long long)c * blk + lo + off;
     }
     s = 0;
+    if (direct && p == n - 1) {  // the block is already in place
+      if (len > 0) dskip += (len + slice - 1) / slice;
+      s = len;
+    }
   }
   __device__ __forceinline__ bool next(SliceDesc& d) {
     while (true) {

@@ -105,6 +105,7 @@ __device__ __forceinline__ void consumeVectors(int ct, int CT, int nv, const cha
 template <class It>
 __device__ __forceinline__ long long directSkipped(const It&) { return 0; }
 __device__ __forceinline__ long long directSkipped(const RingIter& it) { return it.dskip; }
+__device__ __forceinline__ long long directSkipped(const PhaseIter& it) { return it.dskip; }
 
 // DIRECT: the ring's all-gather through the recv buffers (F_DRECV /
 // F_DSEND slices); a separate instantiation, so the FIFO form carries none

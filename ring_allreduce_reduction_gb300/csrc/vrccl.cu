@@ -54,6 +54,17 @@ const void* groupKernelFor(int proto, int dtype, int op) {
   return nullptr;
 }
 
+int maxDynamicSmem(const void* fn, int device) {
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return optin - int(fa.sharedSizeBytes);
+}
+
 const void* kernelFor(int algo, int proto, int dtype, int op) {
   if (dtype < 0 || dtype >= vrcclNumTypes || op < 0 || op >= 5) return nullptr;
   const bool x = dtype >= 4;  // the second half of a split table
@@ -394,9 +405,7 @@ static int residentCapacity(const vrcclComm* c, const void* fn, int threads, siz
   if (smem > 0) {
     static std::vector<const void*> raised;
     if (std::find(raised.begin(), raised.end(), fn) == raised.end()) {
-      int optin = 0;
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, maxDynamicSmem(fn, c->device));
       cudaGetLastError();
       raised.push_back(fn);
     }
@@ -771,7 +780,8 @@ static vrcclResult_t runCall(vrcclComm_t comm, const Call& k) {
   ka.scale = 1.0f / (float)n;
   ka.stages = s.stages;
   ka.prefetch = s.P == kSimple ? comm->envPrefetch : 0;
-  ka.direct = comm->direct && s.A == kRing && s.P == kSimple && k.coll == kAllReduce && n > 1;
+  ka.direct = comm->direct && s.A == kRing && s.P == kSimple && (k.coll == kAllReduce || k.coll == kAllGather) &&
+              n > 1;
   for (int r = 0; r < n; ++r) {
     ka.send[r] = k.send[r];
     ka.recv[r] = k.recv[r];

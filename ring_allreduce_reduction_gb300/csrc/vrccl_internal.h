@@ -160,6 +160,10 @@ __host__ __device__ inline int treeDownEdge(int ch, int c, int n, int maxCh) { r
 // Kernel table (defined by the kernel translation units).
 // Returns the __global__ function for (algo, proto, dtype, op) or nullptr.
 const void* kernelFor(int algo, int proto, int dtype, int op);
+// Largest dynamic shared memory a block of kernel `fn` may request on
+// `device`: the opt-in per-block limit less the kernel's static shared
+// memory, which counts against the same limit.
+int maxDynamicSmem(const void* fn, int device);
 // The grouped ring kernel for (proto, dtype, op), or nullptr.
 const void* groupKernelFor(int proto, int dtype, int op);
 

@@ -65,17 +65,17 @@ vrcclResult_t setupDevice(int dev, unsigned char** scratch, unsigned long long* 
       cudaGetLastError();
       return vrcclCudaError;
     }
-    int sms = 0, optin = 0;
+    int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // The same limit the communicator path sets for these kernels, so
-    // neither path lowers it for the other.
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     for (int dt = 0; dt < vrcclNumTypes; ++dt) {
       for (int op = 0; op < vrcclNumOps; ++op) {
         const void* fn = kernelFor(kRing, kSimple, dt, op);
         int per = 0;
         if (!fn ||
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024) != cudaSuccess ||
+            // the same limit the communicator path sets for these kernels,
+            // so neither path lowers it for the other
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, maxDynamicSmem(fn, dev)) !=
+                cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, kNoAllocThreads, kNoAllocSmem) !=
                 cudaSuccess ||
             per * sms < kNoAllocMaxEdges) {

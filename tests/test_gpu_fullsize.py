@@ -90,6 +90,10 @@ def test_bench_workload_fp32_256MiB(v):
         torch.cuda.synchronize()
         sched = _sampled_check(v, comm, x, recv, "float32", "sum")
         assert sched["proto"] == "simple" and sched["nchannels"] >= 16
+        # the full Simple agent shape is reachable: 32 KiB slices need the
+        # kernel's dynamic shared memory raised past the 48 KiB default
+        shape = v.vrcclCommGetLaunchShape(comm)
+        assert shape["slice_elems"] * 4 == 32768 and shape["blocks"] == 8 * sched["nchannels"], shape
     finally:
         v.vrcclCommDestroy(comm)
 

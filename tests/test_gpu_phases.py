@@ -60,9 +60,13 @@ class Rows:
         return bool(np.all(h[:, :GUARD] == CANARY) and np.all(h[:, GUARD + self.nbytes:] == CANARY))
 
 
+INT_RANGE = {"int32": (-2**20, 2**20), "int8": (-128, 127), "uint8": (0, 255), "int64": (-2**62, 2**62)}
+
+
 def _inputs(n, count, dtype, op, seed=0):
-    if dtype == "int32":
-        return make_inputs(n, count, dtype, "int_uniform", seed=seed, lo=-2**20, hi=2**20)
+    if dtype in INT_RANGE:
+        lo, hi = INT_RANGE[dtype]
+        return make_inputs(n, count, dtype, "int_uniform", seed=seed, lo=lo, hi=hi)
     if op == "prod":
         return make_inputs(n, count, dtype, "uniform", seed=seed, lo=0.5, hi=2.0)
     return make_inputs(n, count, dtype, "normal", seed=seed)
@@ -175,6 +179,29 @@ def test_all_gather_is_the_concatenation(v, proto, n):
                 want = phases.ring_all_gather(x)
                 assert np.array_equal(y.view(np.uint8), want.view(np.uint8)), (dtype, inplace)
                 assert ok
+    finally:
+        v.vrcclCommDestroy(comm)
+
+
+@pytest.mark.parametrize("direct", [True, False])
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_all_gather_both_forms(v, n, direct):
+    """Simple AllGather with its blocks moved through the recv buffers (the
+    default) and through the FIFOs: 3 channels and 256-byte chunks (several
+    loops and a short last one), 1-, 2-, 4- and 8-byte types, in place and
+    not, several launches on one communicator."""
+    comm = v.vrcclCommInit(n, 4)
+    try:
+        v.vrcclCommSetDirect(comm, direct)
+        v.vrcclCommSetSchedule(comm, 3, 256)
+        for dtype, b in (("bfloat16", 8 * 777), ("float32", 4 * 1001), ("int8", 16 * 301), ("float64", 2 * 999)):
+            for inplace in (False, True):
+                x = _inputs(n, b, dtype, "sum", seed=b + n)
+                y, ok = _ag(v, comm, x, dtype, "simple", inplace)
+                want = phases.ring_all_gather(x)
+                assert np.array_equal(y.view(np.uint8), want.view(np.uint8)), (dtype, inplace)
+                assert ok
+        assert v.vrcclCommGetAsyncError(comm) == 0
     finally:
         v.vrcclCommDestroy(comm)
 
