@@ -360,9 +360,9 @@ vrcclResult_t vrcclModelPredict(const vrcclModelGraph_t* graph, vrcclAlgo_t algo
  * bit-identical to the FIFO form, which moves (6n-4) S bytes through the
  * SMs against the direct form's (5n-4) S. A standalone AllGather moves
  * each block the same way: written into the next rank's recv buffer, then
- * forwarded from there. 0 (or VRCCL_DIRECT=0 at vrcclCommInit) selects the
- * FIFO all-gather. LL, LL128, the tree, ReduceScatter and grouped launches
- * always use the FIFOs.
+ * forwarded from there; grouped AllReduces do the same task by task. 0 (or
+ * VRCCL_DIRECT=0 at vrcclCommInit) selects the FIFO all-gather. LL, LL128,
+ * the tree and ReduceScatter always use the FIFOs.
  * Errors: vrcclInvalidArgument (bad handle, enable not 0 or 1).
  */
 vrcclResult_t vrcclCommSetDirect(vrcclComm_t comm, int enable);

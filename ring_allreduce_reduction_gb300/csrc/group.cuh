@@ -1,7 +1,9 @@
 // Grouped AllReduce: one launch runs a list of ring AllReduces of one type
 // and op. Each channel's agents walk the tasks that use their channel in
 // task order, so the two ends of every ring edge see the same sequence of
-// slices and the FIFO counters simply continue from task to task.
+// slices and the FIFO counters simply continue from task to task; so do
+// the direct all-gather's counters (Simple), whose forwarded chunks land in
+// the next rank's buffer of the same task.
 #pragma once
 
 #include "kernels.cuh"
@@ -20,7 +22,9 @@ struct GroupRingIter {
   const char* out0;
   RingIter it;
   long long dIn, dOut;
-  bool live;
+  long long dNext;     // direct: next rank's task buffer against its task-0 one, less dOut (elements)
+  long long skipDone;  // direct: slices passed over in finished tasks
+  bool live, direct;
 
   __device__ __forceinline__ void init(const GroupArgs* g_, int n_, int r_, int ch_) {
     g = g_;
@@ -32,9 +36,12 @@ struct GroupRingIter {
     slice = g->sliceElems;
     in0 = reinterpret_cast<const char*>(g->send[r]);
     out0 = reinterpret_cast<const char*>(g->recv[r]);
-    dIn = dOut = 0;
+    dIn = dOut = dNext = skipDone = 0;
     live = false;
+    direct = g->direct != 0 && n > 1;
   }
+  __device__ __forceinline__ long long skippedDirect() const { return skipDone + (live ? it.dskip : 0); }
+  __device__ __forceinline__ long long nextShift() const { return dNext; }
   __device__ __forceinline__ bool nextTask() {
     const int C = g->nchannels;
     while (++t < g->ntasks) {
@@ -43,9 +50,12 @@ struct GroupRingIter {
       if (j >= T.nch) continue;
       unsigned long long lo, hi;
       channelRange<S>(T.count, T.nch, j, lo, hi);
-      it.init(n, r, (long long)lo, (long long)(hi - lo), K, 16 / (long long)sizeof(S), slice);
+      it.init(n, r, (long long)lo, (long long)(hi - lo), K, 16 / (long long)sizeof(S), slice, direct);
       dIn = (reinterpret_cast<const char*>(g->send[t * n + r]) - in0) / (long long)sizeof(S);
       dOut = (reinterpret_cast<const char*>(g->recv[t * n + r]) - out0) / (long long)sizeof(S);
+      const int r1 = (r + 1) % n;
+      dNext = (reinterpret_cast<const char*>(g->recv[t * n + r1]) - reinterpret_cast<const char*>(g->recv[r1])) /
+                  (long long)sizeof(S) - dOut;
       return true;
     }
     return false;
@@ -57,6 +67,8 @@ struct GroupRingIter {
         d.outPos += dOut;
         return true;
       }
+      if (live) skipDone += it.dskip;
+      live = false;
       if (!nextTask()) return false;
       live = true;
     }
@@ -78,7 +90,18 @@ __global__ void __launch_bounds__(maxAgentThreads(PROTO)) groupRingKernel(const 
   }
   GroupRingIter<S> it;
   it.init(&g, n, r, ch);
-  ringAgent<PROTO, DT, OP>(g, ag, it, reinterpret_cast<const char*>(g.send[r]), reinterpret_cast<char*>(g.recv[r]));
+  const char* in = reinterpret_cast<const char*>(g.send[r]);
+  char* out = reinterpret_cast<char*>(g.recv[r]);
+  if constexpr (PROTO == kSimple) {
+    if (it.direct) {
+      ag.addDirect(c, ringEdge(ch, (r - 1 + n) % n, n), ringEdge(ch, r, n));
+      ringAgent<PROTO, DT, OP, true>(g, ag, it, in, out);
+    } else {
+      ringAgent<PROTO, DT, OP, false>(g, ag, it, in, out);
+    }
+  } else {
+    ringAgent<PROTO, DT, OP>(g, ag, it, in, out);
+  }
 }
 
 #define VRCCL_GROUP_ROW(PROTO, DT)                                                          \

@@ -90,6 +90,10 @@ struct RingIter {
       s = cHi;
     }
   }
+  // direct: slices passed over so far, and where a slice sits in the next
+  // rank's recv buffer relative to its position here (the same place)
+  __device__ __forceinline__ long long skippedDirect() const { return dskip; }
+  __device__ __forceinline__ long long nextShift() const { return 0; }
   __device__ __forceinline__ void setLoop() {
     rem = chCount - off;
     const long long loop = (long long)n * K;
@@ -175,6 +179,8 @@ struct PhaseIter {
     p = 0;
     flags = 0;
   }
+  __device__ __forceinline__ long long skippedDirect() const { return dskip; }
+  __device__ __forceinline__ long long nextShift() const { return 0; }
   __device__ __forceinline__ void setChunk() {
     int c;
     if (!gather) {
@@ -227,6 +233,8 @@ struct PhaseIter {
 struct TreeIter {
   long long lo, chCount, slice, s;
   int flags;
+  __device__ __forceinline__ long long skippedDirect() const { return 0; }
+  __device__ __forceinline__ long long nextShift() const { return 0; }
   __device__ __forceinline__ void init(long long lo_, long long chCount_, long long slice_, int flags_) {
     lo = lo_;
     chCount = chCount_;

@@ -100,17 +100,10 @@ __device__ __forceinline__ void consumeVectors(int ct, int CT, int nv, const cha
   }
 }
 
-// Direct all-gather slices of the passed-over last steps (RingIter::dskip);
-// other sequences have none.
-template <class It>
-__device__ __forceinline__ long long directSkipped(const It&) { return 0; }
-__device__ __forceinline__ long long directSkipped(const RingIter& it) { return it.dskip; }
-__device__ __forceinline__ long long directSkipped(const PhaseIter& it) { return it.dskip; }
-
 // DIRECT: the ring's all-gather through the recv buffers (F_DRECV /
 // F_DSEND slices); a separate instantiation, so the FIFO form carries none
 // of its per-slice work. The in-edge's count of direct slices received is
-// the slices run (ag.drstep) plus those passed over (directSkipped).
+// the slices run (ag.drstep) plus those passed over (it.skippedDirect()).
 template <int DT, int OP, bool TREE, bool DIRECT = false, class Args, class It>
 __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, char* out) {
   using S = typename Ty<DT>::S;
@@ -249,7 +242,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
         // buffer; take its whole 16-byte units (the ragged end of the
         // buffer is read element by element, never past the buffer).
         const unsigned long long before = dtailSeen;
-        ok = flagAtLeast(c, ag, &c.dctrl[ag.dre].tail, ag.drstep + directSkipped(it) + 1, dtailSeen, 0);
+        ok = flagAtLeast(c, ag, &c.dctrl[ag.dre].tail, ag.drstep + it.skippedDirect() + 1, dtailSeen, 0);
         const unsigned dBytes = unsigned(d.nelem * E / 16 * 16);
         if (ok && dBytes) {
           if (dtailSeen != before) fenceProxyAsync();
@@ -327,7 +320,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
     }
     // The direct in-edge's head is read only at the next launch's start
     // (it seeds that launch's count), so it is written once, complete.
-    if constexpr (DIRECT) redMaxRelaxed(&c.dctrl[ag.dre].head, ag.drstep + directSkipped(it));
+    if constexpr (DIRECT) redMaxRelaxed(&c.dctrl[ag.dre].head, ag.drstep + it.skippedDirect());
     return;
   }
 
@@ -351,7 +344,7 @@ __device__ void simplePipeline(const Args& a, Agent& ag, It it, const char* in, 
     const int rf = d.flags | (drv ? F_RECV : 0);  // the reduction sees a received value
     char* dst0 = (d.flags & F_SEND) && ag.nsend > 0 ? ag.slot(c, ag.se[0], ag.sstep[0]) : nullptr;
     char* dst1 = (d.flags & F_SEND) && ag.nsend > 1 ? ag.slot(c, ag.se[1], ag.sstep[1]) : nullptr;
-    char* dnx = DIRECT && (d.flags & F_DSEND) ? nextOut + d.outPos * E : nullptr;
+    char* dnx = DIRECT && (d.flags & F_DSEND) ? nextOut + (d.outPos + it.nextShift()) * E : nullptr;
     char* o = out + d.outPos * E;
     const int nv = d.nelem / V;
     {

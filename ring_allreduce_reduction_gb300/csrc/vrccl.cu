@@ -883,6 +883,7 @@ static vrcclResult_t launchRuns(vrcclComm_t comm, const std::vector<Call>& calls
     g->sliceElems = sliceElems;
     g->stages = s.stages;
     g->prefetch = s.P == kSimple ? comm->envPrefetch : 0;
+    g->direct = comm->direct && s.P == kSimple && n > 1;
     g->scale = 1.0f / (float)n;
     std::vector<double> load(s.C, 0.0);
     unsigned long long steps = 0;

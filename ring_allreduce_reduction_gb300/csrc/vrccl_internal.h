@@ -145,6 +145,7 @@ struct GroupArgs {
   int sliceElems;  // elements per FIFO step
   int stages;      // Simple: shared-memory stages
   int prefetch;    // Simple: input L2 prefetch distance (0 = off)
+  int direct;      // Simple: all-gather through the recv buffers
   int ntasks;
   float scale;     // avg pre-scale 1.0f / n
   GroupTask task[kMaxGroupTasks];

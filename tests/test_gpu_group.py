@@ -57,11 +57,16 @@ def _oracle_ar(x, dtype, op, s):
     return oring.ring_allreduce(x, op, dtype, s["nchannels"], s["chunk_elems"])
 
 
-def test_mixed_group_matches_oracle_and_aggregation_rule(v):
+@pytest.mark.parametrize("direct", [True, False])
+def test_mixed_group_matches_oracle_and_aggregation_rule(v, direct):
+    """Both all-gather forms: through the recv buffers (the default; every
+    call's buffers are separate tensors, so the next rank's buffer of a task
+    sits at its own offset) and through the FIFOs."""
     import torch
     n = 8
     comm = v.vrcclCommInit(n, 32)
     try:
+        v.vrcclCommSetDirect(comm, direct)
         spec = [  # (dtype, op, count, algo, proto)
             ("float32", "sum", 300_000, "auto", "auto"),
             ("float32", "sum", 100_001, "ring", "auto"),      # within 4x of the first: same run
