@@ -13,15 +13,18 @@
 //                        slice q is drained and its in-edge slot filled
 //                        (cached flag values cover several slices per
 //                        poll), then, once stage q % S is free, bulk-copies
-//                        the received slot(s) next to the input.
+//                        the received slot(s) next to the input; in the
+//                        direct all-gather, the chunk the predecessor wrote
+//                        into this rank's recv buffer instead.
 //   warp 2, one thread   publisher: once every consumer warp is past a run
 //                        of slices it publishes them with one gpu-scope fence
 //                        and the new tail (sent) and head (drained) counters.
 //   warps 3..W+2         consumers. They wait for the stage, reduce from
 //                        shared memory, store the result to the out-edge
-//                        slot and/or the recv buffer, free the stage and
-//                        report the slice done. They never fence at gpu
-//                        scope, so no consumer waits for the memory system.
+//                        slot, the recv buffer and/or (direct) the next
+//                        rank's recv buffer, free the stage and report the
+//                        slice done. They never fence at gpu scope, so no
+//                        consumer waits for the memory system.
 //
 // So the producer keeps up to S slices of input and FIFO data in flight
 // while consumers work, and no CTA-wide barrier is taken per slice.
