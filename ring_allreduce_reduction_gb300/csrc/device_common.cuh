@@ -63,6 +63,13 @@ __device__ __forceinline__ uint4 ldStream16(const void* p) { return __ldcs(reint
 __device__ __forceinline__ void stStream16(void* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
 __device__ __forceinline__ uint4 ldFifo16(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ void stFifo16(void* p, uint4 v) { __stcg(reinterpret_cast<uint4*>(p), v); }
+// A FIFO store under an L2 policy (evictLastPolicy below): the slot stays in
+// L2 until its receiver has read and dropped it.
+__device__ __forceinline__ void stFifoHint16(void* p, uint4 v, unsigned long long policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ uint2 ldStream8(const void* p) { return __ldcs(reinterpret_cast<const uint2*>(p)); }
 __device__ __forceinline__ void stStream8(void* p, uint2 v) { __stcs(reinterpret_cast<uint2*>(p), v); }
 __device__ __forceinline__ uint2 ldFifo8(const void* p) { return __ldcg(reinterpret_cast<const uint2*>(p)); }
@@ -112,6 +119,11 @@ __device__ __forceinline__ void bulkLoad(void* dstSmem, const void* srcGlobal, u
 // The same copy, tagged to be evicted from L2 first: for data read once
 // (an agent's own input), so it does not push out FIFO lines that are still
 // to be read.
+__device__ __forceinline__ unsigned long long evictLastPolicy() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ unsigned long long evictFirstPolicy() {
   unsigned long long pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
