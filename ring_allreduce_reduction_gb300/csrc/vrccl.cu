@@ -586,7 +586,7 @@ static vrcclResult_t chooseShape(vrcclComm_t comm, int coll, int algo, int proto
     SimpleShape sh;
     // 2-byte types do twice the element arithmetic per byte: with a large
     // share per agent they take twice the consumer warps (measured on the
-    // bf16 avg bucket, 1 GiB per rank: 16 warps 3.57 ms, 8 warps 3.61 ms;
+    // bf16 avg bucket, 1 GiB per rank: 16 warps 3.40 ms, 8 warps 3.47 ms;
     // before the ring's consumer loop was compiled per slice kind 5.1 and
     // 6.2 ms; the bf16 sum at 256 MiB is 3 % faster with 8, fp32 2 %
     // slower with 16). Below 1 MiB per agent the larger block only adds
