@@ -596,8 +596,8 @@ def main() -> int:
                     help="allreduce only: the schedule timed (the workload's is the ring)")
     ap.add_argument("--no-bound", action="store_true", help="skip timing the one-shot bound beside the ring")
     ap.add_argument("--fifo", action="store_true",
-                    help="ring AllReduce with its all-gather through the FIFOs (the library's default runs it "
-                         "through the recv buffers)")
+                    help="ring AllReduce / AllGather with the all-gather through the FIFOs (the library's default "
+                         "runs it through the recv buffers)")
     ap.add_argument("--bucket", default="", choices=["", "flat", "group", "separate"],
                     help="time the 224-tensor bf16 gradient bucket instead of the workload")
     ap.add_argument("--proto", default="", choices=["", "simple", "ll", "ll128"],
@@ -785,6 +785,8 @@ def main() -> int:
                    "algo": sched["algo"], "proto": sched["proto"], "channels": sched["nchannels"],
                    "chunk_elems": sched["chunk_elems"], "blocks": shape["blocks"], "threads": shape["threads"],
                    "slice_elems": shape["slice_elems"],
+                   "allgather": ("through the FIFOs" if args.fifo or coll == "reduce_scatter" or sched["algo"] != "ring"
+                                 or sched["proto"] != "simple" else "through the recv buffers (direct)"),
                    "l2": "inputs larger than L2 (n*S = 2 GiB in, 2 GiB out); no flush",
                    "algbw_gbs": round(S / (ms_step / 1e3) / 1e9 * world, 3),
                    "parallelism": (f"one problem split over {world} GPUs by element range (vrcclShardRange); "
