@@ -785,7 +785,8 @@ def main() -> int:
                    "algo": sched["algo"], "proto": sched["proto"], "channels": sched["nchannels"],
                    "chunk_elems": sched["chunk_elems"], "blocks": shape["blocks"], "threads": shape["threads"],
                    "slice_elems": shape["slice_elems"],
-                   "allgather": ("through the FIFOs" if args.fifo or coll == "reduce_scatter" or sched["algo"] != "ring"
+                   "allgather": ("none (one-shot)" if sched["algo"] == "oneshot" else
+                                 "through the FIFOs" if args.fifo or coll == "reduce_scatter" or sched["algo"] != "ring"
                                  or sched["proto"] != "simple" else "through the recv buffers (direct)"),
                    "l2": "inputs larger than L2 (n*S = 2 GiB in, 2 GiB out); no flush",
                    "algbw_gbs": round(S / (ms_step / 1e3) / 1e9 * world, 3),
