@@ -405,7 +405,10 @@ static int residentCapacity(const vrcclComm* c, const void* fn, int threads, siz
   if (smem > 0) {
     static std::vector<const void*> raised;
     if (std::find(raised.begin(), raised.end(), fn) == raised.end()) {
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, maxDynamicSmem(fn, c->device));
+      const int want = maxDynamicSmem(fn, c->device);
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, want) != cudaSuccess && c->debug)
+        // the launch still runs, in the smaller shapes that fit the default
+        fprintf(stderr, "vrccl: could not raise a kernel's dynamic shared memory to %d bytes\n", want);
       cudaGetLastError();
       raised.push_back(fn);
     }
